@@ -1,0 +1,17 @@
+"""GB300 (sm_103a) single-query decode attention: dense, paged and sparse.
+
+The compute lives in hand-written CUDA kernels behind a C ABI (``include/decode_attn.h``,
+``libdecode_attn.so``); :mod:`.binding` marshals torch tensors into those calls.  Importing
+this package does not load the library; the first call does, and raises if it was not built.
+"""
+_BINDING_NAMES = (
+    "DecodeAttnError", "abi_version", "decode_attn_dense", "decode_attn_paged",
+    "decode_attn_sparse", "decode_attn_workspace_size", "library_path", "load_library",
+)
+
+
+def __getattr__(name):
+    if name in _BINDING_NAMES:
+        from . import binding
+        return getattr(binding, name)
+    raise AttributeError(name)
