@@ -1,0 +1,455 @@
+"""Decode-attention benchmark: achieved HBM GB/s (and % of the measured GB300 copy peak) and
+µs per call, on one of the named synthetic workloads.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one decode-attention call over the whole workload (one kernel launch; inputs resident
+in HBM).  The live K/V bytes of every workload but the small ones exceed L2, and two
+independent input copies are alternated between steps, so no step reads what the previous one
+left in L2.  With N > 1 (torchrun), every rank runs its own replica of the workload with its
+own seed; the job value is the bytes of all ranks over the slowest rank's time.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (a bounded sample).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from token_decode_attention_split_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and µs per call"
+DEFAULT_WORKLOAD = "dense_batched"
+KERNEL_SOURCES = ["token_decode_attention_split_gb300/csrc/decode_kernel.cuh",
+                  "token_decode_attention_split_gb300/csrc/ptx.cuh"]
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def traffic_record(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when it was taken on other
+    kernel sources than the ones built now."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d.get(workload)
+        if rec and rec.get("kernel_sha") == kernel_sha():
+            return float(rec["bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def gpu_selector(dev) -> str:
+    """nvidia-smi -i argument for the torch device: its UUID when torch reports one."""
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev.index or 0)
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_case(name: str, device, seed_offset: int = 0):
+    cfg = dict(W.CONFIGS[name])
+    return W.make(name, device=device, seed=cfg["seed"] + seed_offset)
+
+
+def case_bytes_copied(case):
+    """Host->device bytes of one end-to-end step: the buffers the step reads."""
+    if case.kind == "dense":
+        live = 2 * case.B * case.Hkv * case.k_len * case.D * 2
+        return case.q.numel() * 2 + live
+    if case.kind == "paged":
+        return (case.q.numel() * 2 + 2 * case.k_pool.numel() * 2 + case.block_table.numel() * 4
+                + case.kv_args.numel() * 4)
+    return case.q.numel() * 2 + 2 * case.k_pool.numel() * 2 + case.sel.numel() * 4
+
+
+class HostCopy:
+    """Pinned host copies of one case's inputs and the per-step H2D / D2H copies of the
+    end-to-end measurement (dense: the live rows of each (b, kv-head) as one strided copy)."""
+
+    def __init__(self, case):
+        self.case = case
+        import ctypes
+        self.rt = ctypes.CDLL("libcudart.so.13")
+        self.rt.cudaMemcpy2DAsync.restype = ctypes.c_int
+        self.rt.cudaMemcpy2DAsync.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                              ctypes.c_size_t, ctypes.c_size_t, ctypes.c_size_t,
+                                              ctypes.c_int, ctypes.c_void_p]
+        c = case
+        if c.kind == "dense":
+            self.q = c.q.cpu().pin_memory()
+            self.k = c.k[:, :, :c.k_len].contiguous().cpu().pin_memory()
+            self.v = c.v[:, :, :c.k_len].contiguous().cpu().pin_memory()
+        elif c.kind == "paged":
+            self.q = c.q.cpu().pin_memory()
+            self.k = c.k_pool.cpu().pin_memory()
+            self.v = c.v_pool.cpu().pin_memory()
+            self.bt = c.block_table.cpu().pin_memory()
+            self.kl = c.kv_args.cpu().pin_memory()
+        else:
+            self.q = c.q.cpu().pin_memory()
+            self.k = c.k_pool.cpu().pin_memory()
+            self.v = c.v_pool.cpu().pin_memory()
+            self.sel = c.sel.cpu().pin_memory()
+        self.out = torch.empty(c.out_shape(), dtype=torch.bfloat16).pin_memory()
+
+    def h2d(self, stream):
+        c = self.case
+        s = stream.cuda_stream
+        c.q.copy_(self.q, non_blocking=True)
+        if c.kind == "dense":
+            rows = c.B * c.Hkv
+            width = c.k_len * c.D * 2
+            pitch = c.capacity * c.D * 2
+            for dst, src in ((c.k, self.k), (c.v, self.v)):
+                rc = self.rt.cudaMemcpy2DAsync(dst.data_ptr(), pitch, src.data_ptr(), width,
+                                               width, rows, 1, s)
+                if rc != 0:
+                    raise RuntimeError(f"cudaMemcpy2DAsync failed ({rc})")
+        elif c.kind == "paged":
+            c.k_pool.copy_(self.k, non_blocking=True)
+            c.v_pool.copy_(self.v, non_blocking=True)
+            c.block_table.copy_(self.bt, non_blocking=True)
+            c.kv_args.copy_(self.kl, non_blocking=True)
+        else:
+            c.k_pool.copy_(self.k, non_blocking=True)
+            c.v_pool.copy_(self.v, non_blocking=True)
+            c.sel.copy_(self.sel, non_blocking=True)
+
+    def d2h(self, out):
+        self.out.copy_(out, non_blocking=True)
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "native" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def dist_max(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def oracle_sample_run(case_host, budget_s: float):
+    """Runs the oracle on as many (b, h) rows of the workload as fit in about ``budget_s``
+    seconds (whole passes when they fit); returns (rows, seconds, threads)."""
+    import oracle
+    n = case_host.B * case_host.Hq
+    threads = os.cpu_count() or 1
+    # size the sample from a short probe
+    probe = np.arange(min(n, max(1, threads)), dtype=np.int64)
+    t0 = time.perf_counter()
+    _run_oracle(case_host, probe, threads)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    per_row = dt / len(probe)
+    rows = int(max(1, min(n, budget_s / per_row)))
+    pairs = np.linspace(0, n - 1, rows).round().astype(np.int64)
+    pairs = np.unique(pairs)
+    t0 = time.perf_counter()
+    _run_oracle(case_host, pairs, threads)
+    return len(pairs), time.perf_counter() - t0, threads
+
+
+def _run_oracle(c, pairs, threads):
+    import oracle
+    if c.kind == "dense":
+        return oracle.dense(c.q, c.k, c.v, c.k_len, c.scale, pairs=pairs, nthreads=threads)
+    if c.kind == "paged":
+        return oracle.paged(c.q, c.k_pool, c.v_pool, c.block_table.numpy(),
+                            c.kv_args.numpy().view(np.uint32), c.scale,
+                            kv_len_stride=c.kv_len_stride, pairs=pairs, nthreads=threads)
+    return oracle.sparse(c.q, c.k_pool, c.v_pool, c.sel.numpy(), c.scale, pairs=pairs,
+                         nthreads=threads)
+
+
+def cpu_case(name):
+    """The workload built on the host (seeded like the GPU run; for the large pools the host
+    draw is slow, so it is drawn on the GPU when one is present and copied back)."""
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    c = make_case(name, dev)
+    if dev == "cpu":
+        return c
+    for f in ("q", "k", "v", "k_pool", "v_pool", "block_table", "kv_args", "sel"):
+        if hasattr(c, f):
+            setattr(c, f, getattr(c, f).cpu())
+    torch.cuda.empty_cache()
+    return c
+
+
+def cpu_baseline(name: str, budget_s: float = 15.0):
+    c = cpu_case(name)
+    rows, secs, threads = oracle_sample_run(c, budget_s)
+    frac = rows / (c.B * c.Hq)
+    gbs = c.algorithmic_bytes() * frac / secs / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} of {c.B * c.Hq} (b, h) rows of {name} in {secs:.2f} s; "
+                      f"value = that share of the workload's algorithmic bytes / time"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    name = args.workload
+    c = cpu_case(name)
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    times = []
+    rows_used = 0
+    threads = os.cpu_count() or 1
+    for i in range(args.warmup + args.steps):
+        rows, secs, threads = oracle_sample_run(c, per_step)
+        if i >= args.warmup:
+            times.append(secs / rows)
+            rows_used = rows
+    per_row = float(np.mean(times))
+    secs_full = per_row * c.B * c.Hq
+    gbs = c.algorithmic_bytes() / secs_full / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs_full * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{rows_used} of {c.B * c.Hq} (b, h) rows per step, scaled "
+                                   f"to the whole workload"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_native(args, world, rank, local):
+    from token_decode_attention_split_gb300 import binding as B_
+    B_.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    name = args.workload
+    cases = [make_case(name, dev, seed_offset=1000 * rank + k) for k in range(2)]
+    c0 = cases[0]
+    var = {"dense": 0, "paged": 1, "sparse": 2}[c0.kind]
+    ws = B_.new_workspace(B_.decode_attn_workspace_size(
+        var, c0.B, c0.Hq, c0.Hkv, c0.D, getattr(c0, "width", 0)), dev)
+    outs = [torch.empty(c.out_shape(), dtype=torch.bfloat16, device=dev) for c in cases]
+    stream = torch.cuda.Stream(dev)
+    alg = [c.algorithmic_bytes() for c in cases]
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            B_.run_case(cases[i % 2], out=outs[i % 2], workspace=ws, stream=stream)
+    stream.synchronize()
+
+    # ---- timed region: K back-to-back calls, events on the launching stream
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(gpu_selector(dev))
+    clocks.start()
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            starts[i].record(stream)
+            B_.run_case(cases[i % 2], out=outs[i % 2], workspace=ws, stream=stream)
+            ends[i].record(stream)
+    stream.synchronize()
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = starts[0].elapsed_time(ends[-1])
+    step_ms = dist_max(total_ms / args.steps, world, dev)
+    launch_ms = float(np.mean(per_launch_ms))
+    bytes_step = float(np.mean([alg[i % 2] for i in range(args.steps)]))
+
+    # ---- end to end: pinned host inputs copied in and the output copied back every step
+    hc = [HostCopy(c) for c in cases]
+    h2d = case_bytes_copied(c0)
+    d2h = outs[0].numel() * 2
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 20))
+    with torch.cuda.stream(stream):
+        hc[0].h2d(stream)
+        B_.run_case(cases[0], out=outs[0], workspace=ws, stream=stream)
+        hc[0].d2h(outs[0])
+    stream.synchronize()
+    dist_barrier(world)
+    with torch.cuda.stream(stream):
+        e_start.record(stream)
+        for i in range(e2e_steps):
+            hc[i % 2].h2d(stream)
+            B_.run_case(cases[i % 2], out=outs[i % 2], workspace=ws, stream=stream)
+            hc[i % 2].d2h(outs[i % 2])
+        e_end.record(stream)
+    stream.synchronize()
+    e2e_ms = dist_max(e_start.elapsed_time(e_end) / e2e_steps, world, dev)
+
+    peak, peak_kind = measured_peak()
+    value = world * bytes_step / (step_ms * 1e-3) / 1e9
+    achieved = bytes_step / (launch_ms * 1e-3) / 1e9
+    traffic = traffic_record(name)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "us_per_call": round(step_ms * 1e3, 2),
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": name, **{k: v for k, v in W.CONFIGS[name].items() if k != "seed"},
+                   "algorithmic_bytes_per_call": int(bytes_step),
+                   "l2": "inputs larger than L2; two input copies alternated",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": f"decode_attn_kernel<{c0.kind}>",
+                     "launch_us": round(launch_ms * 1e3, 2)},
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(name, args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.CONFIGS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_native(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

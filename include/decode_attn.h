@@ -1,0 +1,142 @@
+/*
+ * decode_attn.h -- C ABI of the GB300 (sm_103a) single-query decode-attention library.
+ *
+ * One query row per (sequence b, query head h) attends a KV cache with softmax_scale and GQA
+ * grouping (query head h reads KV head h / (Hq / Hkv)).  There is no ALiBi, no sliding window
+ * and no logit softcap, and causal masking is not a parameter: with one query row it changes
+ * nothing ("DecodeFlashSpec", fuel_dispatch::decode_flash, fields alibi / causal /
+ * window_size_left / window_size_right / softcap).  Three forms:
+ *   decode_attn_dense   rows [0, k_len) of a capacity buffer      (DecodeFlashSpec, k / v / k_len)
+ *   decode_attn_paged   per-sequence kv_len read on the device from an args buffer, rows gathered
+ *                       through a block table       ("DflashScratch", option_b_indirect_args_dev)
+ *   decode_attn_sparse  a fixed-width int32 selection whose -1 pads add exactly nothing
+ *                       ("AttnV41", decode_fixed_topk / decode_prep)
+ *
+ * Conventions shared by every entry point
+ *   - Element type: every q / k / v / out buffer holds bfloat16 values (2 bytes each); the
+ *     arithmetic is fp32 (scores, online softmax, accumulation), the output is rounded to bf16
+ *     round-to-nearest-even.
+ *   - Pointers: q, k, v, pools, out, block_table, kv_lens, sel and the workspace are DEVICE
+ *     pointers of the current CUDA device, owned by the caller; q, k, v, pools, out and the
+ *     workspace must be 16-byte aligned, block_table / kv_lens / sel 4-byte aligned.
+ *   - Layouts are dense row-major with D contiguous:
+ *       q, out          [B, Hq, 1, D]
+ *       dense k, v      [B, Hkv, capacity, D]
+ *       paged pools     [num_pages, Hkv, page_size, D]   (one page of one KV head is contiguous)
+ *       block_table     int32 [B, max_pages_per_seq]
+ *       kv_lens         u32 words; sequence b's kv_len is kv_lens[b * kv_len_stride]
+ *       sparse pools    [B, Hkv, pool_rows, D]
+ *       sel             int32 [B, width], shared by every KV head of a sequence
+ *   - Supported: D in {64, 128}; 1 <= Hq / Hkv <= 64.  Other shapes return DA_ERR_UNSUPPORTED
+ *     (fail closed, nothing launched).
+ *   - Streams: a call only enqueues kernels on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  It allocates nothing, frees nothing and never synchronises, so it can be
+ *     captured in a CUDA graph; the tensor-map descriptors and launch arguments it builds are
+ *     baked into the launch.
+ *   - Values that live on the device (kv_lens, block_table, sel) are never checked by a
+ *     device-to-host copy.  They are handled on the device: kv_len is clamped to
+ *     max_pages_per_seq * page_size; a row whose block-table entry lies outside [0, num_pages),
+ *     and a selection entry outside [0, pool_rows) (-1 or any other), is skipped; an empty row
+ *     set (k_len = 0, kv_len = 0, an all-pad selection) yields a zero output row.
+ *   - Errors: the return value is checked on the host before anything is enqueued; on any
+ *     status other than DA_OK nothing was launched and `out` is untouched.
+ *   - Workspace: caller-owned device scratch of at least decode_attn_workspace_size() bytes.
+ *     It must be zero-filled once before its first use (decode_attn_workspace_init or
+ *     cudaMemset); every completed call leaves its counters at zero again, so later calls need
+ *     no clearing.  One workspace must not be shared by calls that can run concurrently.
+ */
+#ifndef DECODE_ATTN_H
+#define DECODE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DECODE_ATTN_ABI_VERSION 1
+
+typedef enum {
+    DA_OK = 0,
+    DA_ERR_INVALID_ARGUMENT = 1,   /* null/misaligned pointer, bad shape or length, bad scale */
+    DA_ERR_UNSUPPORTED = 2,        /* valid request outside the kernels' shape support */
+    DA_ERR_WORKSPACE_TOO_SMALL = 3,
+    DA_ERR_CUDA = 4                /* a CUDA runtime call or kernel launch failed */
+} da_status;
+
+typedef enum { DA_VARIANT_DENSE = 0, DA_VARIANT_PAGED = 1, DA_VARIANT_SPARSE = 2 } da_variant;
+
+/* DECODE_ATTN_ABI_VERSION of the built library. */
+int decode_attn_abi_version(void);
+
+/* Static, human-readable text for a da_status value (never NULL). */
+const char *decode_attn_status_string(int status);
+
+/* Workspace bytes a call of `variant` needs on the current device for these shapes.
+ * max_kv is the selection width for DA_VARIANT_SPARSE and is ignored otherwise.
+ * Returns 0 for arguments the calls would reject. */
+size_t decode_attn_workspace_size(int variant, int B, int Hq, int Hkv, int D, int64_t max_kv);
+
+/* Zero-fills `bytes` of a workspace on `stream` (cudaMemsetAsync). */
+da_status decode_attn_workspace_init(void *workspace, size_t bytes, void *stream);
+
+/*
+ * Dense decode attention over the live prefix of a capacity buffer.
+ * Follows "DecodeFlashSpec" (docs.rs fuel_dispatch::decode_flash): q [B,Hq,1,D] attends rows
+ * [0, k_len) of k, v [B,Hkv,capacity,D]; k_len is the live length cached_len + seq
+ * (field k_len, resolved to a concrete value per call); rows at or past k_len are never read.
+ *   0 <= k_len <= capacity, capacity >= 1; k_len = 0 writes zeros.
+ *   softmax_scale: finite; typically 1/sqrt(D) (field softmax_scale).
+ */
+da_status decode_attn_dense(const void *q, const void *k, const void *v, void *out, int B, int Hq,
+                            int Hkv, int D, int64_t capacity, int64_t k_len, float softmax_scale,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Paged decode attention with per-sequence lengths read on the device.
+ * Follows "DflashScratch" (docs.metrale.ai dflash_head), field option_b_indirect_args_dev: the
+ * kernel reads kv_len of sequence b at entry from kv_lens[b * kv_len_stride]; stride 3 reads
+ * the first word of the 12-byte record {u32 kv_len, u32 q_offset, u32 q_rope_pos}, stride 1 a
+ * plain u32 array.  Row j of sequence b is slot j % page_size of page block_table[b][j /
+ * page_size].  The pointer stays fixed while the host rewrites the values between launches.
+ *   page_size: a power of two in [8, 256]; max_pages_per_seq >= 1; 1 <= num_pages < 2^31;
+ *   kv_len_stride in {1, 3}; B <= 1024.
+ */
+da_status decode_attn_paged(const void *q, const void *k_pool, const void *v_pool, void *out,
+                            const int32_t *block_table, int max_pages_per_seq, int page_size,
+                            int64_t num_pages, const uint32_t *kv_lens, int kv_len_stride, int B,
+                            int Hq, int Hkv, int D, float softmax_scale, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
+ * Sparse decode attention over a fixed-width selection.
+ * Follows "AttnV41" (docs.metrale.ai attn_v41), methods decode_fixed_topk and decode_prep: each
+ * sequence's selection lists pool rows (window slots, then the shared index selection, then -1
+ * pads up to the fixed width); each valid entry adds its row once (duplicates count once per
+ * entry); a -1 entry adds an exact zero to the denominator and nothing to the output.
+ * Appending -1 pads to a selection leaves every output bit unchanged (the work is split into
+ * fixed 256-entry chunks that do not depend on width, B or the device).
+ *   1 <= pool_rows < 2^31; width >= 0 (width = 0 writes zeros).
+ */
+da_status decode_attn_sparse(const void *q, const void *k_pool, const void *v_pool, void *out,
+                             int64_t pool_rows, const int32_t *sel, int width, int B, int Hq,
+                             int Hkv, int D, float softmax_scale, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/* Caps the number of CTAs the dense and paged calls spread their work over (0 = one per SM,
+ * the default).  Process-wide; a smaller grid gives every KV head more split segments, which
+ * exercises the cross-CTA log-sum-exp merge.  Returns DA_ERR_INVALID_ARGUMENT for a negative
+ * value. */
+da_status decode_attn_set_grid_limit(int max_ctas);
+
+/* Reads and clears the device error word of the current device (synchronises the device).
+ * A kernel whose bounded wait on a pipeline barrier timed out (about one second) stops its
+ * work, records a nonzero code here and returns instead of hanging; 0 means no such event. */
+da_status decode_attn_read_device_error(uint32_t *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_ATTN_H */

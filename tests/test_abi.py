@@ -1,0 +1,123 @@
+"""The C ABI on the host, no GPU needed: every symbol the header declares is exported, and
+arguments the calls must reject are rejected before anything touches the device."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+
+import pytest
+
+from token_decode_attention_split_gb300 import binding, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "decode_attn.h")
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+FAKE = 0x10000          # an aligned non-null address the rejected calls never dereference
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(decode_attn_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("decode_attn_dense", "decode_attn_paged", "decode_attn_sparse",
+              "decode_attn_workspace_size", "decode_attn_abi_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_version_and_status_strings(lib):
+    src = open(HEADER).read()
+    ver = int(re.search(r"#define DECODE_ATTN_ABI_VERSION (\d+)", src).group(1))
+    assert lib.decode_attn_abi_version() == ver
+    for s in range(5):
+        assert lib.decode_attn_status_string(s)
+    assert lib.decode_attn_status_string(99) == b"unknown status"
+
+
+def dense(lib, q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=1, Hq=8, Hkv=2, D=128, cap=16, k_len=8,
+          scale=0.1, ws=FAKE, ws_bytes=1 << 20):
+    return lib.decode_attn_dense(q, k, v, out, B, Hq, Hkv, D, cap, k_len, scale, ws, ws_bytes, None)
+
+
+def paged(lib, B=2, Hq=8, Hkv=2, D=128, P=16, maxp=4, npages=16, stride=1, bt=FAKE, kl=FAKE,
+          q=FAKE, scale=0.1):
+    return lib.decode_attn_paged(q, FAKE, FAKE, FAKE, bt, maxp, P, npages, kl, stride, B, Hq, Hkv,
+                                 D, scale, FAKE, 1 << 20, None)
+
+
+def sparse(lib, B=2, Hq=8, Hkv=1, D=128, R=100, width=10, sel=FAKE, scale=0.1):
+    return lib.decode_attn_sparse(FAKE, FAKE, FAKE, FAKE, R, sel, width, B, Hq, Hkv, D, scale, FAKE,
+                                  1 << 20, None)
+
+
+def test_dense_rejects(lib):
+    assert dense(lib, q=None) == INVALID
+    assert dense(lib, k=None) == INVALID
+    assert dense(lib, ws=None) == INVALID
+    assert dense(lib, q=FAKE + 2) == INVALID            # misaligned
+    assert dense(lib, Hq=6, Hkv=4) == INVALID            # Hq % Hkv != 0
+    assert dense(lib, k_len=17) == INVALID               # k_len > capacity
+    assert dense(lib, k_len=-1) == INVALID
+    assert dense(lib, cap=0, k_len=0) == INVALID
+    assert dense(lib, scale=math.nan) == INVALID
+    assert dense(lib, scale=math.inf) == INVALID
+    assert dense(lib, D=96) == UNSUPPORTED               # fail closed
+    assert dense(lib, D=256) == UNSUPPORTED
+    assert dense(lib, Hq=128, Hkv=1) == UNSUPPORTED      # group of 128 heads
+    assert dense(lib, cap=1 << 31, k_len=5) == UNSUPPORTED
+    assert dense(lib, B=0) == OK                         # empty batch: nothing to do
+
+
+def test_paged_rejects(lib):
+    assert paged(lib, bt=None) == INVALID
+    assert paged(lib, kl=None) == INVALID
+    assert paged(lib, kl=FAKE + 2) == INVALID
+    assert paged(lib, stride=2) == INVALID
+    assert paged(lib, maxp=0) == INVALID
+    assert paged(lib, npages=0) == INVALID
+    assert paged(lib, P=12) == UNSUPPORTED
+    assert paged(lib, P=4) == UNSUPPORTED
+    assert paged(lib, P=512) == UNSUPPORTED
+    assert paged(lib, B=1025) == UNSUPPORTED
+    assert paged(lib, D=80) == UNSUPPORTED
+    assert paged(lib, B=0) == OK
+
+
+def test_sparse_rejects(lib):
+    assert sparse(lib, width=-1) == INVALID
+    assert sparse(lib, R=0) == INVALID
+    assert sparse(lib, sel=None) == INVALID
+    assert sparse(lib, sel=FAKE + 1) == INVALID
+    assert sparse(lib, R=1 << 31) == UNSUPPORTED
+    assert sparse(lib, Hq=65, Hkv=1) == UNSUPPORTED
+    assert sparse(lib, B=0) == OK
+
+
+def test_misc_host_calls(lib):
+    assert lib.decode_attn_set_grid_limit(-1) == INVALID
+    assert lib.decode_attn_set_grid_limit(0) == OK
+    assert lib.decode_attn_workspace_init(None, 0, None) == OK
+    assert lib.decode_attn_workspace_init(None, 16, None) == INVALID
+    assert lib.decode_attn_read_device_error(None) == INVALID
+    # sizes the calls would reject have no workspace size
+    assert lib.decode_attn_workspace_size(0, 1, 6, 4, 128, 0) == 0
+    assert lib.decode_attn_workspace_size(2, 1, 8, 1, 96, 10) == 0
+    assert lib.decode_attn_workspace_size(7, 1, 8, 1, 128, 10) == 0

@@ -1,0 +1,126 @@
+"""GPU dense decode attention against the fp64 oracle ("DecodeFlashSpec", fields q / k / v /
+k_len / softmax_scale): every output element within 1e-2 + 1e-2 |ref|."""
+import numpy as np
+import pytest
+import torch
+
+from token_decode_attention_split_gb300 import binding as B_
+from token_decode_attention_split_gb300 import workloads as W
+
+from helpers import assert_close, bits, oracle_for, out_f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _reset_grid():
+    B_.decode_attn_set_grid_limit(0)
+    yield
+    B_.decode_attn_set_grid_limit(0)
+
+
+SHAPES = [
+    # B, Hq, Hkv, D, capacity, k_len   (several 64-row tiles, ragged tails, every group size)
+    (1, 8, 2, 64, 512, 300),
+    (2, 8, 8, 128, 300, 257),      # G = 1
+    (3, 4, 2, 64, 200, 129),       # G = 2
+    (2, 32, 8, 128, 700, 640),     # G = 4, exact multiple of the tile
+    (2, 64, 8, 128, 1000, 777),    # G = 8
+    (1, 32, 2, 128, 500, 333),     # G = 16
+    (2, 32, 1, 64, 400, 190),      # G = 32
+    (2, 64, 1, 128, 300, 201),     # G = 64
+    (1, 12, 2, 128, 100, 65),      # G = 6 (padded group)
+    (1, 40, 1, 128, 100, 99),      # G = 40 (padded group)
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "B{}_Hq{}_Hkv{}_D{}_cap{}_k{}".format(*s))
+def test_dense_matches_oracle(shape):
+    B, Hq, Hkv, D, cap, k_len = shape
+    c = W.make_dense(B, Hq, Hkv, D, cap, k_len, seed=100 + k_len, device=DEV, k_scale=2.0,
+                     poison_tail=True)
+    out = B_.run_case(c)
+    assert_close(out_f64(out), oracle_for(c), f"dense {shape}")
+
+
+@pytest.mark.parametrize("limit", [1, 2, 3, 7, 19])
+def test_dense_forced_split_merge(limit):
+    """Few CTAs: each (b, kv-head) is cut into several segments merged by log-sum-exp."""
+    B_.decode_attn_set_grid_limit(limit)
+    c = W.make_dense(2, 16, 2, 128, 1100, 1037, seed=7, device=DEV, k_scale=2.0, poison_tail=True)
+    out = B_.run_case(c)
+    assert_close(out_f64(out), oracle_for(c), f"grid limit {limit}")
+
+
+def test_klen_one_returns_v0_exactly():
+    c = W.make_dense(2, 16, 2, 128, 64, 1, seed=8, device=DEV, poison_tail=True)
+    out = B_.run_case(c)
+    v0 = c.v[:, :, 0:1, :].repeat_interleave(8, dim=1)          # [B, Hq, 1, D]
+    assert torch.equal(out, v0)
+
+
+def test_klen_zero_gives_zeros():
+    c = W.make_dense(2, 8, 2, 64, 32, 0, seed=9, device=DEV)
+    out = torch.full(c.out_shape(), 7.0, dtype=torch.bfloat16, device=DEV)
+    B_.run_case(c, out=out)
+    assert torch.count_nonzero(out).item() == 0
+
+
+def test_identical_keys_give_mean_of_v():
+    c = W.make_dense(2, 32, 4, 128, 600, 555, seed=10, device=DEV)
+    c.k[:] = c.k[:, :, :1, :]
+    out = B_.run_case(c)
+    mean = c.v[:, :, :c.k_len].double().mean(dim=2).repeat_interleave(8, dim=1)
+    assert_close(out_f64(out), mean.cpu().numpy(), "identical keys")
+
+
+def test_deterministic_and_stream_ordered():
+    c = W.make_dense(2, 64, 8, 128, 2000, 1999, seed=11, device=DEV)
+    s = torch.cuda.Stream()
+    ws = B_.new_workspace(B_.decode_attn_workspace_size(0, c.B, c.Hq, c.Hkv, c.D), DEV)
+    B_.decode_attn_set_grid_limit(5)
+    with torch.cuda.stream(s):
+        a = B_.run_case(c, workspace=ws, stream=s)
+        b = B_.run_case(c, workspace=ws, stream=s)
+    s.synchronize()
+    assert torch.equal(a, b)
+    assert torch.count_nonzero(ws[: 4 * c.B * c.Hkv]).item() == 0   # counters back at zero
+
+
+def test_workspace_too_small_is_rejected():
+    c = W.make_dense(1, 8, 2, 64, 64, 64, seed=12, device=DEV)
+    need = B_.decode_attn_workspace_size(0, c.B, c.Hq, c.Hkv, c.D)
+    ws = B_.new_workspace(need, DEV)
+    out = torch.empty(c.out_shape(), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(B_.DecodeAttnError) as e:
+        B_.decode_attn_dense(c.q, c.k, c.v, out, c.k_len, c.scale, ws[: need - 16])
+    assert e.value.status == 3
+
+
+@pytest.mark.parametrize("name", ["dense_tiny", "dense_batched", "dense_long"])
+def test_dense_named_workloads(name):
+    """Full sizes: sampled (b, h) rows against the oracle, every row checked for properties that
+    hold at any size (finite, inside the per-column range of the attended V rows)."""
+    c = W.make(name, device=DEV)
+    out = B_.run_case(c)
+    torch.cuda.synchronize()
+    got = out_f64(out)
+    n = c.B * c.Hq
+    rng = np.random.default_rng(0)
+    pairs = np.unique(np.concatenate([[0, n - 1], rng.choice(n, size=min(n, 24), replace=False)]))
+    host = W.DenseCase(c.q.cpu(), c.k.cpu(), c.v.cpu(), c.k_len, c.scale, c.B, c.Hq, c.Hkv, c.D,
+                       c.capacity)
+    ref = oracle_for(host, pairs=pairs)
+    assert_close(got.reshape(n, -1)[pairs], ref.reshape(n, -1)[pairs], name)
+    assert np.all(np.isfinite(got))
+    G = c.Hq // c.Hkv
+    live = c.v[:, :, :c.k_len].float()
+    lo = live.amin(dim=2).repeat_interleave(G, dim=1).double().cpu().numpy()
+    hi = live.amax(dim=2).repeat_interleave(G, dim=1).double().cpu().numpy()
+    slack = 1e-2 * np.maximum(np.abs(lo), np.abs(hi)) + 1e-3
+    assert np.all(got >= lo - slack) and np.all(got <= hi + slack)
+
+
+def test_no_device_error_recorded():
+    assert B_.decode_attn_read_device_error() == 0

@@ -6,7 +6,10 @@ this package does not load the library; the first call does, and raises if it wa
 """
 _BINDING_NAMES = (
     "DecodeAttnError", "abi_version", "decode_attn_dense", "decode_attn_paged",
-    "decode_attn_sparse", "decode_attn_workspace_size", "library_path", "load_library",
+    "decode_attn_sparse", "decode_attn_workspace_size", "decode_attn_workspace_init",
+    "decode_attn_set_grid_limit", "decode_attn_read_device_error", "library_path",
+    "load_library", "new_workspace", "run_case",
+    "DA_VARIANT_DENSE", "DA_VARIANT_PAGED", "DA_VARIANT_SPARSE",
 )
 
 

@@ -1,0 +1,178 @@
+"""ctypes binding of ``libdecode_attn.so`` (the C ABI in ``include/decode_attn.h``).
+
+Argument marshalling only: tensors become device pointers, shapes become ints, the current
+torch stream becomes the cudaStream_t.  Every step of the computation runs in the library's
+CUDA kernels; there is no fallback, and a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+DA_VARIANT_DENSE, DA_VARIANT_PAGED, DA_VARIANT_SPARSE = 0, 1, 2
+_lock = threading.Lock()
+_lib = None
+
+
+class DecodeAttnError(RuntimeError):
+    def __init__(self, status: int, what: str, text: str):
+        super().__init__(f"{what}: {text} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library() -> ctypes.CDLL:
+    """Loads the built library; raises if it has not been built (``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(f"decode-attention CUDA library not built: {path} is missing")
+        lib = ctypes.CDLL(path)
+        vp, sz, i, i64, f = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        lib.decode_attn_abi_version.restype = i
+        lib.decode_attn_abi_version.argtypes = []
+        lib.decode_attn_status_string.restype = ctypes.c_char_p
+        lib.decode_attn_status_string.argtypes = [i]
+        lib.decode_attn_workspace_size.restype = sz
+        lib.decode_attn_workspace_size.argtypes = [i, i, i, i, i, i64]
+        lib.decode_attn_workspace_init.restype = i
+        lib.decode_attn_workspace_init.argtypes = [vp, sz, vp]
+        lib.decode_attn_dense.restype = i
+        lib.decode_attn_dense.argtypes = [vp, vp, vp, vp, i, i, i, i, i64, i64, f, vp, sz, vp]
+        lib.decode_attn_paged.restype = i
+        lib.decode_attn_paged.argtypes = [vp, vp, vp, vp, vp, i, i, i64, vp, i, i, i, i, i, f, vp,
+                                          sz, vp]
+        lib.decode_attn_sparse.restype = i
+        lib.decode_attn_sparse.argtypes = [vp, vp, vp, vp, i64, vp, i, i, i, i, i, f, vp, sz, vp]
+        lib.decode_attn_set_grid_limit.restype = i
+        lib.decode_attn_set_grid_limit.argtypes = [i]
+        lib.decode_attn_read_device_error.restype = i
+        lib.decode_attn_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        _lib = lib
+        return lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        text = load_library().decode_attn_status_string(status).decode()
+        raise DecodeAttnError(status, what, text)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def abi_version() -> int:
+    return load_library().decode_attn_abi_version()
+
+
+def decode_attn_workspace_size(variant: int, B: int, Hq: int, Hkv: int, D: int, max_kv: int = 0) -> int:
+    return int(load_library().decode_attn_workspace_size(variant, B, Hq, Hkv, D, max_kv))
+
+
+def decode_attn_workspace_init(workspace: torch.Tensor, stream=None):
+    _check(load_library().decode_attn_workspace_init(
+        _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream, workspace.device)), "decode_attn_workspace_init")
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zero-filled workspace buffer (16-byte aligned torch allocation)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def decode_attn_set_grid_limit(max_ctas: int):
+    _check(load_library().decode_attn_set_grid_limit(int(max_ctas)), "decode_attn_set_grid_limit")
+
+
+def decode_attn_read_device_error() -> int:
+    code = ctypes.c_uint32(0)
+    _check(load_library().decode_attn_read_device_error(ctypes.byref(code)),
+           "decode_attn_read_device_error")
+    return int(code.value)
+
+
+def _dims_q(q):
+    if q.dim() != 4 or q.shape[2] != 1:
+        raise ValueError("q must be [B, Hq, 1, D]")
+    return q.shape[0], q.shape[1], q.shape[3]
+
+
+def decode_attn_dense(q, k, v, out, k_len: int, softmax_scale: float, workspace, stream=None):
+    """q, out [B,Hq,1,D]; k, v [B,Hkv,capacity,D]; all bf16 CUDA tensors, contiguous."""
+    B, Hq, D = _dims_q(q)
+    Hkv, cap = k.shape[1], k.shape[2]
+    _check(load_library().decode_attn_dense(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, D, cap, int(k_len), float(softmax_scale),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream, q.device)),
+        "decode_attn_dense")
+    return out
+
+
+def decode_attn_paged(q, k_pool, v_pool, out, block_table, kv_lens, kv_len_stride: int,
+                      softmax_scale: float, workspace, stream=None):
+    """Pools [num_pages,Hkv,page_size,D] bf16; block_table int32 [B,max_pages]; kv_lens int32
+    tensor holding the u32 words (kv_len of sequence b at b * kv_len_stride)."""
+    B, Hq, D = _dims_q(q)
+    num_pages, Hkv, P = k_pool.shape[0], k_pool.shape[1], k_pool.shape[2]
+    _check(load_library().decode_attn_paged(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(out), _ptr(block_table), block_table.shape[1], P,
+        num_pages, _ptr(kv_lens), int(kv_len_stride), B, Hq, Hkv, D, float(softmax_scale),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream, q.device)),
+        "decode_attn_paged")
+    return out
+
+
+def decode_attn_sparse(q, k_pool, v_pool, out, sel, softmax_scale: float, workspace, stream=None):
+    """Pools [B,Hkv,pool_rows,D] bf16; sel int32 [B,width]."""
+    B, Hq, D = _dims_q(q)
+    Hkv, R = k_pool.shape[1], k_pool.shape[2]
+    _check(load_library().decode_attn_sparse(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(out), R, _ptr(sel), sel.shape[1], B, Hq, Hkv, D,
+        float(softmax_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream, q.device)), "decode_attn_sparse")
+    return out
+
+
+def run_case(case, out=None, workspace=None, stream=None):
+    """Runs one workload object (``workloads.DenseCase`` / ``PagedCase`` / ``SparseCase``) through
+    the matching entry point, allocating the output and a zeroed workspace when not given."""
+    dev = case.q.device
+    if out is None:
+        out = torch.empty(case.out_shape(), dtype=torch.bfloat16, device=dev)
+    if case.kind == "dense":
+        if workspace is None:
+            workspace = new_workspace(decode_attn_workspace_size(
+                DA_VARIANT_DENSE, case.B, case.Hq, case.Hkv, case.D), dev)
+        return decode_attn_dense(case.q, case.k, case.v, out, case.k_len, case.scale, workspace,
+                                 stream)
+    if case.kind == "paged":
+        if workspace is None:
+            workspace = new_workspace(decode_attn_workspace_size(
+                DA_VARIANT_PAGED, case.B, case.Hq, case.Hkv, case.D), dev)
+        return decode_attn_paged(case.q, case.k_pool, case.v_pool, out, case.block_table,
+                                 case.kv_args, case.kv_len_stride, case.scale, workspace, stream)
+    if case.kind == "sparse":
+        if workspace is None:
+            workspace = new_workspace(decode_attn_workspace_size(
+                DA_VARIANT_SPARSE, case.B, case.Hq, case.Hkv, case.D, case.width), dev)
+        return decode_attn_sparse(case.q, case.k_pool, case.v_pool, out, case.sel, case.scale,
+                                  workspace, stream)
+    raise ValueError(case.kind)

@@ -1,0 +1,396 @@
+// C ABI of the decode-attention library: argument checks, tensor-map descriptors, workspace
+// layout, grid sizing and the kernel launch.  Every path either launches work on the caller's
+// stream or returns an error before anything is enqueued.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "decode_attn.h"
+#include "launch.h"
+
+namespace da {
+
+// Device error word: kernels whose bounded waits time out record a code here.
+__device__ unsigned int g_device_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_grid_limit{0};
+std::mutex g_mu;
+std::set<std::pair<const void*, int>> g_configured;   // (kernel, device) with smem opt-in done
+int g_sm_count[kMaxDevices];                          // 0 = not queried yet
+unsigned* g_err_ptr[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+int sm_count(int dev) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return 0;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+unsigned* device_error_ptr(int dev) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_err_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_device_error_word) != cudaSuccess) return nullptr;
+        g_err_ptr[dev] = static_cast<unsigned*>(ptr);
+    }
+    return g_err_ptr[dev];
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int padded_group(int G) {
+    if (G <= 8) return 8;
+    if (G <= 16) return 16;
+    if (G <= 32) return 32;
+    if (G <= 64) return 64;
+    return 0;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t counters, lse, o, total;
+};
+
+WsLayout ws_layout(long long units, long long segments, int G, int D) {
+    WsLayout w;
+    w.counters = 0;
+    w.lse = round_up(static_cast<size_t>(units) * 4, 256);
+    w.o = w.lse + round_up(static_cast<size_t>(segments) * G * 4, 256);
+    w.total = w.o + static_cast<size_t>(segments) * G * D * 4;
+    if (w.total == 0) w.total = 256;
+    return w;
+}
+
+// Checks shared by every variant; returns DA_OK when the heads, dims and scale are usable.
+da_status check_common(const void* q, const void* out, int B, int Hq, int Hkv, int D, float scale,
+                       const void* ws) {
+    if (!q || !out || !ws) return DA_ERR_INVALID_ARGUMENT;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(ws, 16)) return DA_ERR_INVALID_ARGUMENT;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return DA_ERR_INVALID_ARGUMENT;
+    if (!std::isfinite(scale)) return DA_ERR_INVALID_ARGUMENT;
+    if (D != 64 && D != 128) return DA_ERR_UNSUPPORTED;
+    if (padded_group(Hq / Hkv) == 0) return DA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * Hq * D >= (1ll << 40)) return DA_ERR_UNSUPPORTED;
+    return DA_OK;
+}
+
+Params base_params(const void* q, void* out, int B, int Hq, int Hkv, float scale, unsigned* err) {
+    Params p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = err;
+    return p;
+}
+
+void bind_workspace(Params& p, void* ws, const WsLayout& w) {
+    unsigned char* base = static_cast<unsigned char*>(ws);
+    p.counters = reinterpret_cast<unsigned*>(base + w.counters);
+    p.part_lse = reinterpret_cast<float*>(base + w.lse);
+    p.part_o = reinterpret_cast<float*>(base + w.o);
+}
+
+da_status zero_output(void* out, int B, int Hq, int D, cudaStream_t st) {
+    const size_t bytes = static_cast<size_t>(B) * Hq * D * 2;
+    return cudaMemsetAsync(out, 0, bytes, st) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+bool encode_3d(CUtensorMap* map, const void* base, cuuint64_t d0, cuuint64_t d1, cuuint64_t d2,
+               cuuint64_t stride1_bytes, cuuint64_t stride2_bytes, cuuint32_t box1) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {64, box1, 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// CTAs for a persistent dense/paged launch on `dev`.
+int persistent_ctas(int dev) {
+    const int sms = sm_count(dev);
+    const int lim = g_grid_limit.load();
+    return (lim > 0 && lim < sms) ? lim : sms;
+}
+
+long long sparse_chunks(long long width) { return (width + kSparseChunkKeys - 1) / kSparseChunkKeys; }
+
+}  // namespace
+
+int kernel_smem_bytes(int D, int GP) {
+#define DA_SMEM_CASE(d, g) \
+    if (D == d && GP == g) return Geometry<d, g>::kSmemBytes;
+    DA_SMEM_CASE(64, 8) DA_SMEM_CASE(64, 16) DA_SMEM_CASE(64, 32) DA_SMEM_CASE(64, 64)
+    DA_SMEM_CASE(128, 8) DA_SMEM_CASE(128, 16) DA_SMEM_CASE(128, 32) DA_SMEM_CASE(128, 64)
+#undef DA_SMEM_CASE
+    return 0;
+}
+
+int kernel_stages(int D, int GP) {
+#define DA_ST_CASE(d, g) \
+    if (D == d && GP == g) return Geometry<d, g>::kStages;
+    DA_ST_CASE(64, 8) DA_ST_CASE(64, 16) DA_ST_CASE(64, 32) DA_ST_CASE(64, 64)
+    DA_ST_CASE(128, 8) DA_ST_CASE(128, 16) DA_ST_CASE(128, 32) DA_ST_CASE(128, 64)
+#undef DA_ST_CASE
+    return 0;
+}
+
+cudaError_t launch_kernel(const void* kernel, int smem, const Launch& L) {
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    bool need = false;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        need = g_configured.find({kernel, dev}) == g_configured.end();
+    }
+    if (need) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_configured.insert({kernel, dev});
+    }
+    void* args[] = {const_cast<CUtensorMap*>(&L.tm_k), const_cast<CUtensorMap*>(&L.tm_v),
+                    const_cast<Params*>(&L.p)};
+    return cudaLaunchKernel(kernel, dim3(L.grid), dim3(kThreads), args, static_cast<size_t>(smem),
+                            L.stream);
+}
+
+}  // namespace da
+
+using namespace da;
+
+extern "C" {
+
+int decode_attn_abi_version(void) { return DECODE_ATTN_ABI_VERSION; }
+
+const char* decode_attn_status_string(int status) {
+    switch (status) {
+        case DA_OK: return "ok";
+        case DA_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case DA_ERR_UNSUPPORTED: return "unsupported shape or option";
+        case DA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case DA_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+size_t decode_attn_workspace_size(int variant, int B, int Hq, int Hkv, int D, int64_t max_kv) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || (D != 64 && D != 128)) return 0;
+    const int G = Hq / Hkv;
+    if (padded_group(G) == 0) return 0;
+    const long long units = static_cast<long long>(B) * Hkv;
+    long long segments = 0;
+    if (variant == DA_VARIANT_DENSE || variant == DA_VARIANT_PAGED) {
+        const int dev = current_device();
+        if (dev < 0) return 0;
+        const int sms = sm_count(dev);
+        if (sms <= 0) return 0;
+        segments = units + sms;
+    } else if (variant == DA_VARIANT_SPARSE) {
+        if (max_kv < 0) return 0;
+        segments = units * sparse_chunks(max_kv);
+    } else {
+        return 0;
+    }
+    return ws_layout(units, segments, G, D).total;
+}
+
+da_status decode_attn_workspace_init(void* workspace, size_t bytes, void* stream) {
+    if (!workspace && bytes) return DA_ERR_INVALID_ARGUMENT;
+    if (bytes == 0) return DA_OK;
+    return cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DA_OK
+               : DA_ERR_CUDA;
+}
+
+da_status decode_attn_set_grid_limit(int max_ctas) {
+    if (max_ctas < 0) return DA_ERR_INVALID_ARGUMENT;
+    g_grid_limit.store(max_ctas);
+    return DA_OK;
+}
+
+da_status decode_attn_read_device_error(uint32_t* code) {
+    if (!code) return DA_ERR_INVALID_ARGUMENT;
+    const int dev = current_device();
+    if (dev < 0) return DA_ERR_CUDA;
+    unsigned* ptr = device_error_ptr(dev);
+    if (!ptr) return DA_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return DA_ERR_CUDA;
+    if (cudaMemcpy(&v, ptr, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return DA_ERR_CUDA;
+    if (cudaMemset(ptr, 0, sizeof v) != cudaSuccess) return DA_ERR_CUDA;
+    *code = v;
+    return DA_OK;
+}
+
+da_status decode_attn_dense(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                            int Hkv, int D, int64_t capacity, int64_t k_len, float softmax_scale,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+    da_status st = check_common(q, out, B, Hq, Hkv, D, softmax_scale, workspace);
+    if (st != DA_OK) return st;
+    if (!k || !v || !aligned(k, 16) || !aligned(v, 16)) return DA_ERR_INVALID_ARGUMENT;
+    if (capacity < 1 || k_len < 0 || k_len > capacity) return DA_ERR_INVALID_ARGUMENT;
+    if (capacity >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
+    const long long units = static_cast<long long>(B) * Hkv;
+    const long long tiles = (k_len + kTileKeys - 1) / kTileKeys;
+    if (units * tiles >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (B == 0) return DA_OK;
+    const int dev = current_device();
+    if (dev < 0) return DA_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return DA_ERR_CUDA;
+    const int G = Hq / Hkv, GP = padded_group(G);
+    const WsLayout w = ws_layout(units, units + sms, G, D);
+    if (workspace_bytes < w.total) return DA_ERR_WORKSPACE_TOO_SMALL;
+    if (k_len == 0) return zero_output(out, B, Hq, D, cs);
+
+    Launch L{};
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(D) * 2;
+    if (!encode_3d(&L.tm_k, k, D, k_len, units, row_bytes, row_bytes * capacity, kTileKeys) ||
+        !encode_3d(&L.tm_v, v, D, k_len, units, row_bytes, row_bytes * capacity, kTileKeys))
+        return DA_ERR_CUDA;
+    L.p = base_params(q, out, B, Hq, Hkv, softmax_scale, device_error_ptr(dev));
+    bind_workspace(L.p, workspace, w);
+    L.p.k_len = static_cast<int>(k_len);
+    L.p.dense_tiles = static_cast<int>(tiles);
+    const long long N = units * tiles;
+    L.grid = static_cast<int>(std::min<long long>(persistent_ctas(dev), N));
+    L.stream = cs;
+    return launch_dense(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+da_status decode_attn_paged(const void* q, const void* k_pool, const void* v_pool, void* out,
+                            const int32_t* block_table, int max_pages_per_seq, int page_size,
+                            int64_t num_pages, const uint32_t* kv_lens, int kv_len_stride, int B,
+                            int Hq, int Hkv, int D, float softmax_scale, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    da_status st = check_common(q, out, B, Hq, Hkv, D, softmax_scale, workspace);
+    if (st != DA_OK) return st;
+    if (!k_pool || !v_pool || !aligned(k_pool, 16) || !aligned(v_pool, 16)) return DA_ERR_INVALID_ARGUMENT;
+    if (!block_table || !kv_lens || !aligned(block_table, 4) || !aligned(kv_lens, 4))
+        return DA_ERR_INVALID_ARGUMENT;
+    if (max_pages_per_seq < 1 || page_size < 1 || num_pages < 1) return DA_ERR_INVALID_ARGUMENT;
+    if (kv_len_stride != 1 && kv_len_stride != 3) return DA_ERR_INVALID_ARGUMENT;
+    if (page_size < 8 || page_size > 256 || (page_size & (page_size - 1)) != 0) return DA_ERR_UNSUPPORTED;
+    if (num_pages >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
+    if (B > kMaxPagedBatch) return DA_ERR_UNSUPPORTED;
+    const long long cap = static_cast<long long>(max_pages_per_seq) * page_size;
+    if (cap >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
+    const long long units = static_cast<long long>(B) * Hkv;
+    if (units * ((cap + kTileKeys - 1) / kTileKeys) >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(Hkv) * page_size >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (B == 0) return DA_OK;
+    const int dev = current_device();
+    if (dev < 0) return DA_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return DA_ERR_CUDA;
+    const int G = Hq / Hkv, GP = padded_group(G);
+    const WsLayout w = ws_layout(units, units + sms, G, D);
+    if (workspace_bytes < w.total) return DA_ERR_WORKSPACE_TOO_SMALL;
+
+    Launch L{};
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(D) * 2;
+    const cuuint64_t page_bytes = row_bytes * page_size * Hkv;
+    const cuuint32_t box_rows = static_cast<cuuint32_t>(std::min(page_size, kTileKeys));
+    if (!encode_3d(&L.tm_k, k_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
+                   row_bytes, page_bytes, box_rows) ||
+        !encode_3d(&L.tm_v, v_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
+                   row_bytes, page_bytes, box_rows))
+        return DA_ERR_CUDA;
+    L.p = base_params(q, out, B, Hq, Hkv, softmax_scale, device_error_ptr(dev));
+    bind_workspace(L.p, workspace, w);
+    L.p.block_table = block_table;
+    L.p.max_pages = max_pages_per_seq;
+    L.p.page_size = page_size;
+    L.p.num_pages = static_cast<int>(num_pages);
+    L.p.kv_lens = kv_lens;
+    L.p.kv_stride = kv_len_stride;
+    L.grid = persistent_ctas(dev);
+    L.stream = cs;
+    return launch_paged(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+da_status decode_attn_sparse(const void* q, const void* k_pool, const void* v_pool, void* out,
+                             int64_t pool_rows, const int32_t* sel, int width, int B, int Hq,
+                             int Hkv, int D, float softmax_scale, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    da_status st = check_common(q, out, B, Hq, Hkv, D, softmax_scale, workspace);
+    if (st != DA_OK) return st;
+    if (!k_pool || !v_pool || !aligned(k_pool, 16) || !aligned(v_pool, 16)) return DA_ERR_INVALID_ARGUMENT;
+    if (width < 0 || pool_rows < 1) return DA_ERR_INVALID_ARGUMENT;
+    if (width > 0 && (!sel || !aligned(sel, 4))) return DA_ERR_INVALID_ARGUMENT;
+    if (pool_rows >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
+    const long long units = static_cast<long long>(B) * Hkv;
+    const long long chunks = sparse_chunks(width);
+    if (units * chunks >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (B == 0) return DA_OK;
+    const int dev = current_device();
+    if (dev < 0) return DA_ERR_CUDA;
+    const int G = Hq / Hkv, GP = padded_group(G);
+    const WsLayout w = ws_layout(units, units * chunks, G, D);
+    if (workspace_bytes < w.total) return DA_ERR_WORKSPACE_TOO_SMALL;
+    if (width == 0) return zero_output(out, B, Hq, D, cs);
+
+    Launch L{};
+    L.p = base_params(q, out, B, Hq, Hkv, softmax_scale, device_error_ptr(dev));
+    bind_workspace(L.p, workspace, w);
+    L.p.sel = sel;
+    L.p.width = width;
+    L.p.pool_rows = static_cast<int>(pool_rows);
+    L.p.nchunks = static_cast<int>(chunks);
+    L.p.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
+    L.p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
+    L.grid = static_cast<int>(units * chunks);
+    L.stream = cs;
+    return launch_sparse(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+}  // extern "C"

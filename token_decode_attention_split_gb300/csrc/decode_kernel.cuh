@@ -1,0 +1,777 @@
+// Single-query decode attention on sm_103a: one kernel per call.
+//
+// Work decomposition.  A "unit" is one (sequence b, KV head g); its G = Hq/Hkv query heads are
+// processed together so every K/V row is read from HBM exactly once.  A unit's live rows are cut
+// into 64-row tiles.  Dense and paged calls run a persistent grid (one CTA per SM): the tiles of
+// all units are laid end to end and CTA c takes the contiguous range [c*N/C, (c+1)*N/C), so the
+// load is balanced to one tile whatever the lengths.  Sparse calls give each CTA one fixed
+// 256-entry chunk of one unit's selection (fixed so that trailing -1 pads cannot move a chunk
+// boundary).  Each CTA's piece of a unit is a "segment".
+//
+// Inside a CTA.  Warp 4 is the producer: it streams K and V tiles into a ring of shared-memory
+// stages (TMA tile loads with 128-byte swizzle for dense and paged; cp.async 16-byte gathers with
+// the same swizzle for sparse) and posts a per-stage validity mask.  Warps 0-3 consume: the GQA
+// group sits on the N side of mma.m16n8k16 (S^T = K * Q^T, then O^T += V^T * P^T), so each
+// K/V element read from shared memory feeds all G heads; the online softmax (running max, sum and
+// accumulator) stays in fp32 registers.
+//
+// Merge.  A segment covering a whole unit writes the bf16 output directly.  Otherwise it writes
+// its normalised partial row and log2-sum-exp to the workspace and bumps the unit's counter; the
+// CTA that completes the unit merges all its partials by log-sum-exp in segment order (so the
+// result does not depend on which CTA finishes last) and resets the counter to zero.
+//
+// Safety.  Every wait is bounded (about one second); on timeout the CTA records an error code in
+// the device error word, waits for its own copies in flight and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace da {
+
+constexpr int kTileKeys = 64;                 // K/V rows per pipeline stage
+constexpr int kConsumerWarps = 4;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr int kSparseChunkKeys = 256;
+constexpr int kSparseChunkTiles = kSparseChunkKeys / kTileKeys;
+constexpr int kMaxPagedBatch = 1024;
+constexpr int kSmemBudget = 232448;           // opt-in dynamic shared memory per block
+
+enum : int { kDense = 0, kPaged = 1, kSparse = 2 };
+enum : uint32_t { kErrWaitFull = 1, kErrWaitEmpty = 2, kErrWaitGroup = 3, kErrDrain = 4 };
+
+template <int D, int GP>
+struct Geometry {
+    static_assert(D == 64 || D == 128, "head dim");
+    static_assert(GP == 8 || GP == 16 || GP == 32 || GP == 64, "padded group");
+    static constexpr int kHalves = D / 64;                      // 128-byte swizzle spans
+    static constexpr int kTileBytes = kHalves * kTileKeys * 128;  // one K (or V) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int HS = GP <= 16 ? 1 : GP / 16;           // warps splitting the heads
+    static constexpr int NT = GP / 8 / HS;                      // 8-head n-tiles per warp
+    static constexpr int KS = kConsumerWarps / HS;              // warps splitting a tile's rows
+    static constexpr int MT = kTileKeys / 16 / KS;              // 16-row m-tiles per warp
+    static constexpr int KSTEPS = D / 16;                       // k-steps of S^T = K Q^T
+    static constexpr int DT = D / 16;                           // 16-row d tiles of O^T
+    static constexpr int kMergeFloats = KS * GP * D + 2 * KS * GP;
+    static constexpr int kMiscBytes = 1024;                     // barriers, masks, flags
+    static constexpr int kSchedBytes = (2 * kMaxPagedBatch + 2) * 4;
+    static constexpr int kFixedBytes = kMergeFloats * 4 + kMiscBytes + kSchedBytes;
+    static constexpr int kStagesFit = (kSmemBudget - 1024 - kFixedBytes) / kStageBytes;
+    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kFixedBytes;
+    static_assert(kStages >= 2, "pipeline depth");
+    static_assert(kSmemBytes <= kSmemBudget, "shared memory");
+};
+
+struct Params {
+    const __nv_bfloat16* q;   // [B, Hq, D]
+    __nv_bfloat16* out;       // [B, Hq, D]
+    int B, Hq, Hkv, G;
+    float scale_log2;         // softmax_scale * log2(e)
+    unsigned* counters;       // [B * Hkv] segment counters, zero between calls
+    float* part_o;            // [segments, G, D]
+    float* part_lse;          // [segments, G] (log2 domain)
+    unsigned* err;            // device error word
+    // dense
+    int k_len;
+    int dense_tiles;          // ceil(k_len / 64)
+    // paged
+    const int* block_table;
+    int max_pages, page_size, num_pages;
+    const unsigned* kv_lens;
+    int kv_stride;
+    // sparse
+    const int* sel;
+    int width, pool_rows, nchunks;
+    const __nv_bfloat16* k_pool;
+    const __nv_bfloat16* v_pool;
+};
+
+struct Unit {
+    int b, g, u;
+    int len;    // live rows
+    int nt;     // tiles
+    int base;   // global index of the unit's first tile
+};
+
+struct SmemPtrs {
+    unsigned char* stages;
+    float* merge_o;
+    float* merge_m;
+    float* merge_l;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* group;
+    uint64_t* stage_mask;
+    volatile int* abort;
+    int* last_flag;
+    int* seq_prefix;   // [B + 1] exclusive prefix of per-sequence tiles (paged)
+    int* seq_len;      // [B] live rows per sequence (paged)
+};
+
+template <int D, int GP>
+__device__ __forceinline__ SmemPtrs carve_smem(unsigned char* raw) {
+    using Gm = Geometry<D, GP>;
+    SmemPtrs s;
+    unsigned char* base = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    s.stages = base;
+    unsigned char* p = base + Gm::kStages * Gm::kStageBytes;
+    s.merge_o = reinterpret_cast<float*>(p);
+    s.merge_m = s.merge_o + Gm::KS * GP * D;
+    s.merge_l = s.merge_m + Gm::KS * GP;
+    p += Gm::kMergeFloats * 4;
+    p = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15));
+    s.full = reinterpret_cast<uint64_t*>(p);
+    s.empty = s.full + 8;
+    s.group = s.empty + 8;
+    s.stage_mask = s.group + 1;
+    s.abort = reinterpret_cast<volatile int*>(s.stage_mask + 8);
+    s.last_flag = const_cast<int*>(reinterpret_cast<volatile int*>(s.abort)) + 1;
+    s.seq_prefix = reinterpret_cast<int*>(base + Gm::kStages * Gm::kStageBytes +
+                                          Gm::kMergeFloats * 4 + Gm::kMiscBytes);
+    s.seq_len = s.seq_prefix + kMaxPagedBatch + 2;
+    return s;
+}
+
+__device__ __forceinline__ void record_error(unsigned* err, unsigned code) {
+    if (err) atomicCAS(err, 0u, code);
+}
+
+// Byte offset, inside one K or V tile, of 16-byte chunk c (of D/8) of row r.  Each 64-column
+// half of the tile is [64 rows][128 B] with chunk index XOR (row & 7): the layout a TMA tile load
+// with 128-byte swizzle produces, and the one the sparse gather writes by hand.
+__device__ __forceinline__ uint32_t tile_offset(int r, int c) {
+    return static_cast<uint32_t>((c >> 3) * (kTileKeys * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// ------------------------------------------------------------------ schedule
+template <int VAR>
+struct Schedule {
+    int N;     // tiles in the whole call
+    int C;     // CTAs sharing them
+    int t0, t1;
+};
+
+__device__ __forceinline__ int tile_owner(int t, int N, int C) {
+    // the CTA whose range [c*N/C, (c+1)*N/C) holds tile t
+    return static_cast<int>((static_cast<long long>(t + 1) * C + N - 1) / N) - 1;
+}
+
+__device__ __forceinline__ Unit locate_dense(const Params& p, int t) {
+    Unit U;
+    U.nt = p.dense_tiles;
+    U.u = t / U.nt;
+    U.b = U.u / p.Hkv;
+    U.g = U.u - U.b * p.Hkv;
+    U.len = p.k_len;
+    U.base = U.u * U.nt;
+    return U;
+}
+
+__device__ __forceinline__ Unit locate_paged(const Params& p, const SmemPtrs& sm, int t) {
+    // largest b with seq_prefix[b] * Hkv <= t
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sm.seq_prefix[mid] * p.Hkv <= t) lo = mid; else hi = mid - 1;
+    }
+    Unit U;
+    U.b = lo;
+    U.nt = sm.seq_prefix[lo + 1] - sm.seq_prefix[lo];
+    const int r = t - sm.seq_prefix[lo] * p.Hkv;
+    U.g = r / U.nt;
+    U.u = U.b * p.Hkv + U.g;
+    U.len = sm.seq_len[lo];
+    U.base = sm.seq_prefix[lo] * p.Hkv + U.g * U.nt;
+    return U;
+}
+
+// ------------------------------------------------------------------ consumer warp state
+template <int D, int GP>
+struct ConsumerState {
+    using Gm = Geometry<D, GP>;
+    int lane, hg, kg, gq, qd;
+    uint32_t qf[Gm::KSTEPS][Gm::NT][2];   // Q^T as mma B fragments
+    float o[Gm::DT][Gm::NT][4];           // O^T accumulator fragments
+    float m_run[Gm::NT][2];               // running max (log2 domain) of heads 2qd, 2qd+1
+    float l_run[Gm::NT][2];               // this thread's share of the running sum
+
+    __device__ __forceinline__ void init(int warp, int lane_) {
+        lane = lane_;
+        hg = warp % Gm::HS;
+        kg = warp / Gm::HS;
+        gq = lane >> 2;
+        qd = lane & 3;
+    }
+
+    __device__ __forceinline__ int head_of(int nt, int hc) const {
+        return hg * Gm::NT * 8 + nt * 8 + 2 * qd + hc;
+    }
+
+    __device__ __forceinline__ void load_q(const Params& p, int b, int g) {
+#pragma unroll
+        for (int nt = 0; nt < Gm::NT; ++nt) {
+            const int head = hg * Gm::NT * 8 + nt * 8 + gq;
+            const bool ok = head < p.G;
+            const __nv_bfloat16* row =
+                p.q + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * p.G + (ok ? head : 0)) * D;
+            const uint32_t* row32 = reinterpret_cast<const uint32_t*>(row);
+#pragma unroll
+            for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
+                qf[ks][nt][0] = ok ? __ldg(row32 + (16 * ks + 2 * qd) / 2) : 0u;
+                qf[ks][nt][1] = ok ? __ldg(row32 + (16 * ks + 8 + 2 * qd) / 2) : 0u;
+            }
+        }
+    }
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int dt = 0; dt < Gm::DT; ++dt)
+#pragma unroll
+            for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[dt][nt][e] = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < Gm::NT; ++nt) {
+            m_run[nt][0] = m_run[nt][1] = -CUDART_INF_F;
+            l_run[nt][0] = l_run[nt][1] = 0.f;
+        }
+    }
+
+    // One stage: this warp's MT*16 rows of the tile.  `mask` bit r = row r of the tile is valid.
+    __device__ __forceinline__ void consume(uint32_t k_tile, uint32_t v_tile, uint64_t mask,
+                                            float scale_log2) {
+        constexpr int kRows = Gm::MT * 16;
+        const uint64_t rows_mask = kRows == 64 ? ~0ull : ((1ull << kRows) - 1ull);
+        const uint64_t wmask = (mask >> (kg * kRows)) & rows_mask;
+        if (wmask == 0) return;               // no valid row: the state is unchanged
+        const bool all_valid = wmask == rows_mask;
+        const int row0 = kg * kRows;
+
+        // S^T[row, head] = sum_d K[row, d] * Q[head, d]
+        float s[Gm::MT][Gm::NT][4];
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[mt][nt][e] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt) {
+            const int r = row0 + mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
+                uint32_t a[4];
+                ldmatrix_x4(a, k_tile + tile_offset(r, 2 * ks + (lane >> 4)));
+#pragma unroll
+                for (int nt = 0; nt < Gm::NT; ++nt) mma_bf16_16816(s[mt][nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+            }
+        }
+
+        // scale into the log2 domain; invalid rows -> -inf
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float x = s[mt][nt][e] * scale_log2;
+                    if (!all_valid) {
+                        const int rr = mt * 16 + gq + (e >= 2 ? 8 : 0);
+                        if (!((wmask >> rr) & 1ull)) x = -CUDART_INF_F;
+                    }
+                    s[mt][nt][e] = x;
+                }
+
+        // online softmax update per head column
+#pragma unroll
+        for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+                float mx = -CUDART_INF_F;
+#pragma unroll
+                for (int mt = 0; mt < Gm::MT; ++mt) mx = fmaxf(mx, fmaxf(s[mt][nt][hc], s[mt][nt][hc + 2]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float m_new = fmaxf(m_run[nt][hc], mx);
+                const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+                const float alpha = fast_exp2(m_run[nt][hc] - m_use);
+                m_run[nt][hc] = m_new;
+                l_run[nt][hc] *= alpha;
+#pragma unroll
+                for (int dt = 0; dt < Gm::DT; ++dt) {
+                    o[dt][nt][hc] *= alpha;
+                    o[dt][nt][hc + 2] *= alpha;
+                }
+#pragma unroll
+                for (int mt = 0; mt < Gm::MT; ++mt) {
+                    s[mt][nt][hc] = fast_exp2(s[mt][nt][hc] - m_use);
+                    s[mt][nt][hc + 2] = fast_exp2(s[mt][nt][hc + 2] - m_use);
+                }
+            }
+
+        // P (rounded to bf16; the sum uses the rounded weights) -> P^T B fragments
+        uint32_t pb[Gm::MT][Gm::NT][2];
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < Gm::NT; ++nt) {
+                const uint32_t r0 = pack_bf16x2(s[mt][nt][0], s[mt][nt][1]);  // row gq
+                const uint32_t r1 = pack_bf16x2(s[mt][nt][2], s[mt][nt][3]);  // row gq + 8
+                l_run[nt][0] += bf16_lo_to_f32(r0) + bf16_lo_to_f32(r1);
+                l_run[nt][1] += bf16_hi_to_f32(r0) + bf16_hi_to_f32(r1);
+                pb[mt][nt][0] = movmatrix_trans(r0);
+                pb[mt][nt][1] = movmatrix_trans(r1);
+            }
+
+        // O^T[d, head] += sum_row V[row, d] * P[row, head]
+#pragma unroll
+        for (int mt = 0; mt < Gm::MT; ++mt) {
+            const int r = row0 + mt * 16 + (lane & 7) + ((lane >> 4) << 3);
+            uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
+            if (!all_valid) {
+                const int k0 = mt * 16 + 2 * qd;
+                keep_lo = (((wmask >> k0) & 1ull) ? 0x0000ffffu : 0u) |
+                          (((wmask >> (k0 + 1)) & 1ull) ? 0xffff0000u : 0u);
+                keep_hi = (((wmask >> (k0 + 8)) & 1ull) ? 0x0000ffffu : 0u) |
+                          (((wmask >> (k0 + 9)) & 1ull) ? 0xffff0000u : 0u);
+            }
+#pragma unroll
+            for (int dt = 0; dt < Gm::DT; ++dt) {
+                uint32_t a[4];
+                ldmatrix_x4_trans(a, v_tile + tile_offset(r, 2 * dt + ((lane >> 3) & 1)));
+                if (!all_valid) {   // rows never loaded or past the length may hold NaN
+                    a[0] &= keep_lo;
+                    a[1] &= keep_lo;
+                    a[2] &= keep_hi;
+                    a[3] &= keep_hi;
+                }
+#pragma unroll
+                for (int nt = 0; nt < Gm::NT; ++nt) mma_bf16_16816(o[dt][nt], a, pb[mt][nt][0], pb[mt][nt][1]);
+            }
+        }
+    }
+
+    // Writes this warp's (m, l, O) for its heads into merge slot kg.
+    __device__ __forceinline__ void stash(const SmemPtrs& sm) {
+#pragma unroll
+        for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+                float l = l_run[nt][hc];
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                const int head = head_of(nt, hc);
+                const int slot = kg * GP + head;
+                if (gq == 0) {
+                    sm.merge_m[slot] = m_run[nt][hc];
+                    sm.merge_l[slot] = l;
+                }
+#pragma unroll
+                for (int dt = 0; dt < Gm::DT; ++dt) {
+                    sm.merge_o[slot * D + dt * 16 + gq] = o[dt][nt][hc];
+                    sm.merge_o[slot * D + dt * 16 + gq + 8] = o[dt][nt][hc + 2];
+                }
+            }
+    }
+};
+
+// Consumer-group barrier (128 threads) on an mbarrier, bounded.
+__device__ __forceinline__ bool group_sync(const SmemPtrs& sm, uint32_t& phase, unsigned* err) {
+    mbar_arrive(sm.group);
+    const bool ok = mbar_wait(sm.group, phase, sm.abort, kWaitLimitNs);
+    phase ^= 1u;
+    if (!ok) {
+        *sm.abort = 1;
+        record_error(err, kErrWaitGroup);
+    }
+    return ok;
+}
+
+// Finishes one segment of unit U: merges the key-split warps, then either stores the output or
+// publishes a partial and, in the CTA that completes the unit, merges all partials.
+template <int D, int GP>
+__device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& sm,
+                                               ConsumerState<D, GP>& cs, const Unit& U,
+                                               bool whole, int seg, int first_seg, int nseg,
+                                               uint32_t& gphase) {
+    using Gm = Geometry<D, GP>;
+    const int tid = threadIdx.x;   // 0..127 (consumers)
+    cs.stash(sm);
+    if (!group_sync(sm, gphase, p.err)) return false;
+
+    const size_t out_row0 = (static_cast<size_t>(U.b) * p.Hq + static_cast<size_t>(U.g) * p.G);
+    for (int idx = tid; idx < p.G * D; idx += kConsumerThreads) {
+        const int h = idx / D, d = idx - h * D;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int k = 0; k < Gm::KS; ++k) M = fmaxf(M, sm.merge_m[k * GP + h]);
+        float L = 0.f, O = 0.f;
+        bool first = true;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int k = 0; k < Gm::KS; ++k) {
+                const float mk = sm.merge_m[k * GP + h];
+                if (mk == -CUDART_INF_F) continue;
+                const float w = fast_exp2(mk - M);
+                const float lk = w * sm.merge_l[k * GP + h];
+                const float ok = w * sm.merge_o[(k * GP + h) * D + d];
+                if (first) { L = lk; O = ok; first = false; }
+                else { L += lk; O += ok; }
+            }
+        }
+        const bool empty = !(L > 0.f);
+        const float val = empty ? 0.f : O * (1.0f / L);
+        if (whole) {
+            p.out[(out_row0 + h) * D + d] = __float2bfloat16_rn(val);
+        } else {
+            p.part_o[(static_cast<size_t>(seg) * p.G + h) * D + d] = val;
+            if (d == 0) p.part_lse[static_cast<size_t>(seg) * p.G + h] = empty ? -CUDART_INF_F : M + fast_log2(L);
+        }
+    }
+    if (!whole) {
+        __threadfence();
+        if (!group_sync(sm, gphase, p.err)) return false;
+        if (tid == 0) {
+            const unsigned prev = atomicAdd(p.counters + U.u, 1u);
+            *sm.last_flag = (prev == static_cast<unsigned>(nseg - 1)) ? 1 : 0;
+        }
+        if (!group_sync(sm, gphase, p.err)) return false;
+        if (*sm.last_flag) {
+            __threadfence();
+            for (int idx = tid; idx < p.G * D; idx += kConsumerThreads) {
+                const int h = idx / D, d = idx - h * D;
+                float M = -CUDART_INF_F;
+                int live = 0, only = 0;
+                for (int k = 0; k < nseg; ++k) {
+                    const float l = __ldcg(p.part_lse + static_cast<size_t>(first_seg + k) * p.G + h);
+                    if (l != -CUDART_INF_F) { M = fmaxf(M, l); ++live; only = k; }
+                }
+                float val = 0.f;
+                if (live == 1) {
+                    val = __ldcg(p.part_o + (static_cast<size_t>(first_seg + only) * p.G + h) * D + d);
+                } else if (live > 1) {
+                    float L = 0.f, O = 0.f;
+                    bool first = true;
+                    for (int k = 0; k < nseg; ++k) {
+                        const size_t sk = static_cast<size_t>(first_seg + k);
+                        const float l = __ldcg(p.part_lse + sk * p.G + h);
+                        if (l == -CUDART_INF_F) continue;
+                        const float w = fast_exp2(l - M);
+                        const float ow = w * __ldcg(p.part_o + (sk * p.G + h) * D + d);
+                        if (first) { L = w; O = ow; first = false; }
+                        else { L += w; O += ow; }
+                    }
+                    val = O * (1.0f / L);
+                }
+                p.out[(out_row0 + h) * D + d] = __float2bfloat16_rn(val);
+            }
+            if (tid == 0) p.counters[U.u] = 0u;
+        }
+    }
+    return group_sync(sm, gphase, p.err);
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int VAR, int D, int GP>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const Params p) {
+    using Gm = Geometry<D, GP>;
+    extern __shared__ unsigned char smem_raw[];
+    const SmemPtrs sm = carve_smem<D, GP>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int S = Gm::kStages;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(sm.full + s, VAR == kSparse ? 33u : 1u);
+            mbar_init(sm.empty + s, kConsumerWarps);
+        }
+        mbar_init(sm.group, kConsumerThreads);
+        *sm.abort = 0;
+        *sm.last_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (VAR != kSparse && threadIdx.x == kConsumerThreads) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+
+    // ---- schedule
+    int N = 0, C = 1, t0 = 0, t1 = 0;
+    if (VAR == kPaged) {
+        const int cap = p.max_pages * p.page_size;
+        for (int b = threadIdx.x; b < p.B; b += kThreads) {
+            const unsigned raw = __ldg(p.kv_lens + static_cast<size_t>(b) * p.kv_stride);
+            const int len = raw > static_cast<unsigned>(cap) ? cap : static_cast<int>(raw);
+            sm.seq_len[b] = len;
+            sm.seq_prefix[b + 1] = (len + kTileKeys - 1) / kTileKeys;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            int carry = 0;
+            for (int base = 0; base < p.B; base += 32) {
+                const int b = base + lane;
+                int v = b < p.B ? sm.seq_prefix[b + 1] : 0;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, v, off);
+                    if (lane >= off) v += y;
+                }
+                if (b < p.B) sm.seq_prefix[b + 1] = v + carry;
+                carry += __shfl_sync(0xffffffffu, v, 31);
+            }
+            if (lane == 0) sm.seq_prefix[0] = 0;
+        }
+    }
+    __syncthreads();
+
+    if (VAR == kDense) {
+        N = p.B * p.Hkv * p.dense_tiles;
+        C = gridDim.x;
+    } else if (VAR == kPaged) {
+        N = sm.seq_prefix[p.B] * p.Hkv;
+        C = min(static_cast<int>(gridDim.x), N);
+    }
+    if (VAR != kSparse && static_cast<int>(blockIdx.x) < C && N > 0) {
+        t0 = static_cast<int>(static_cast<long long>(blockIdx.x) * N / C);
+        t1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * N / C);
+    }
+    // sparse: this CTA's chunk of one unit
+    int sp_u = 0, sp_chunk = 0;
+    if (VAR == kSparse) {
+        sp_u = blockIdx.x / p.nchunks;
+        sp_chunk = blockIdx.x - sp_u * p.nchunks;
+        const int ntiles = (p.width + kTileKeys - 1) / kTileKeys;
+        t0 = sp_chunk * kSparseChunkTiles;
+        t1 = min(t0 + kSparseChunkTiles, ntiles);
+    }
+
+    if (warp == kConsumerWarps) {
+        // ================================================================ producer warp
+        int it = 0;
+        bool ok = true;
+        if (VAR == kSparse) {
+            const int b = sp_u / p.Hkv;
+            constexpr int CH = D / 8;                     // 16-byte chunks per row
+            constexpr int kRowsPerInstr = 32 / (2 * CH);  // K and V of 1 (D=128) or 2 (D=64) rows
+            const int sub = lane / (2 * CH);
+            const int w = lane % (2 * CH);
+            const bool isv = w >= CH;
+            const int c = isv ? w - CH : w;
+            const __nv_bfloat16* pool = isv ? p.v_pool : p.k_pool;
+            const int* selrow = p.sel + static_cast<size_t>(b) * p.width;
+            for (int t = t0; t < t1 && ok; ++t, ++it) {
+                const int s = it % S;
+                const uint32_t ph = (it / S) & 1;
+                if (!mbar_wait(sm.empty + s, ph ^ 1u, sm.abort, kWaitLimitNs)) { ok = false; break; }
+                const int key0 = t * kTileKeys;
+                const int i0 = key0 + lane, i1 = key0 + 32 + lane;
+                const int idx0 = i0 < p.width ? __ldg(selrow + i0) : -1;
+                const int idx1 = i1 < p.width ? __ldg(selrow + i1) : -1;
+                const bool v0 = idx0 >= 0 && idx0 < p.pool_rows;
+                const bool v1 = idx1 >= 0 && idx1 < p.pool_rows;
+                const uint64_t mask = static_cast<uint64_t>(__ballot_sync(0xffffffffu, v0)) |
+                                      (static_cast<uint64_t>(__ballot_sync(0xffffffffu, v1)) << 32);
+                unsigned char* tile = sm.stages + s * Gm::kStageBytes + (isv ? Gm::kTileBytes : 0);
+#pragma unroll 4
+                for (int rb = 0; rb < kTileKeys; rb += kRowsPerInstr) {
+                    const int r = rb + sub;
+                    const int idx = __shfl_sync(0xffffffffu, rb < 32 ? idx0 : idx1, r & 31);
+                    const bool valid = (mask >> r) & 1ull;
+                    const __nv_bfloat16* src =
+                        pool + (static_cast<size_t>(sp_u) * p.pool_rows + (valid ? idx : 0)) * D + c * 8;
+                    cp_async_16(tile + tile_offset(r, c), src, valid ? 16u : 0u);
+                }
+                if (lane == 0) sm.stage_mask[s] = mask;
+                cp_async_arrive_noinc(sm.full + s);
+                if (lane == 0) mbar_arrive(sm.full + s);
+            }
+            if (!ok) {
+                cp_async_wait_all();
+                *sm.abort = 1;
+                record_error(p.err, kErrWaitEmpty);
+            }
+        } else {
+            // dense / paged: lane 0 issues TMA; paged uses all lanes to fetch block-table entries
+            const int P = p.page_size;
+            const int box_rows = VAR == kPaged ? min(P, kTileKeys) : kTileKeys;
+            const int pages_per_tile = VAR == kPaged ? (P >= kTileKeys ? 1 : kTileKeys / P) : 1;
+            const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * 128u;
+            int bt_b = -1, bt_base = -1;   // current batch: slots [bt_base, bt_base + 32) of sequence bt_b
+            int bt_cur = -1, bt_nxt = -1;
+            for (int t = t0; t < t1 && ok;) {
+                const Unit U = VAR == kDense ? locate_dense(p, t) : locate_paged(p, sm, t);
+                const int tend = min(t1, U.base + U.nt);
+                const int npages_seq = VAR == kPaged ? (U.len + P - 1) / P : 0;
+                for (; t < tend; ++t, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = (it / S) & 1;
+                    if (!mbar_wait(sm.empty + s, ph ^ 1u, sm.abort, kWaitLimitNs)) { ok = false; break; }
+                    const int j = t - U.base;
+                    const int key0 = j * kTileKeys;
+                    const int nvalid = min(kTileKeys, U.len - key0);
+                    uint64_t mask = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+                    unsigned char* ktile = sm.stages + s * Gm::kStageBytes;
+                    unsigned char* vtile = ktile + Gm::kTileBytes;
+                    if (VAR == kDense) {
+                        if (lane == 0) {
+                            sm.stage_mask[s] = mask;
+                            mbar_arrive_expect_tx(sm.full + s, 2u * Gm::kTileBytes);
+#pragma unroll
+                            for (int h = 0; h < Gm::kHalves; ++h) {
+                                tma_load_3d(ktile + h * kTileKeys * 128, &tm_k, 64 * h, key0, U.u, sm.full + s);
+                                tma_load_3d(vtile + h * kTileKeys * 128, &tm_v, 64 * h, key0, U.u, sm.full + s);
+                            }
+                        }
+                    } else {
+                        const int slot0 = key0 / P;
+                        const int want = slot0 & ~31;
+                        if (U.b != bt_b || want != bt_base) {
+                            const int* row = p.block_table + static_cast<size_t>(U.b) * p.max_pages;
+                            if (U.b == bt_b && want == bt_base + 32) {
+                                bt_cur = bt_nxt;
+                            } else {
+                                const int sl = want + lane;
+                                bt_cur = sl < npages_seq ? __ldg(row + sl) : -1;
+                            }
+                            bt_b = U.b;
+                            bt_base = want;
+                            const int sn = want + 32 + lane;
+                            bt_nxt = sn < npages_seq ? __ldg(row + sn) : -1;
+                        }
+                        const int row_in_page = P > kTileKeys ? key0 % P : 0;
+                        uint32_t page_ok = 0;
+                        int pages[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            pages[i] = __shfl_sync(0xffffffffu, bt_cur, (slot0 - bt_base + i) & 31);
+                            if (i < pages_per_tile && slot0 + i < npages_seq && pages[i] >= 0 &&
+                                pages[i] < p.num_pages)
+                                page_ok |= 1u << i;
+                        }
+                        if (lane == 0) {
+                            uint32_t nloaded = 0;
+                            for (int i = 0; i < pages_per_tile; ++i) {
+                                if (page_ok & (1u << i)) { ++nloaded; continue; }
+                                const uint64_t pm = (box_rows >= 64 ? ~0ull : ((1ull << box_rows) - 1ull)) << (i * box_rows);
+                                mask &= ~pm;
+                            }
+                            sm.stage_mask[s] = mask;
+                            mbar_arrive_expect_tx(sm.full + s, nloaded * 2u * Gm::kHalves * box_bytes);
+                            for (int i = 0; i < pages_per_tile; ++i) {
+                                if (!(page_ok & (1u << i))) continue;
+#pragma unroll
+                                for (int h = 0; h < Gm::kHalves; ++h) {
+                                    const int dst = h * kTileKeys * 128 + i * box_rows * 128;
+                                    tma_load_3d(ktile + dst, &tm_k, 64 * h, U.g * P + row_in_page, pages[i], sm.full + s);
+                                    tma_load_3d(vtile + dst, &tm_v, 64 * h, U.g * P + row_in_page, pages[i], sm.full + s);
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+            if (!ok) {
+                *sm.abort = 1;
+                record_error(p.err, kErrWaitEmpty);
+                if (lane == 0) {
+                    // let every load already issued land before the CTA can exit
+                    for (int k = it - S < 0 ? 0 : it - S; k < it; ++k) {
+                        if (!mbar_wait(sm.full + (k % S), (k / S) & 1, nullptr, kWaitLimitNs)) {
+                            record_error(p.err, kErrDrain);
+                            break;
+                        }
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // ==================================================================== consumer warps
+    ConsumerState<D, GP> cs;
+    cs.init(warp, lane);
+    uint32_t gphase = 0;
+
+    if (VAR == kPaged) {
+        // units with no rows get a zero row (null-row convention)
+        const int units = p.B * p.Hkv;
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            const int b = u / p.Hkv, g = u - b * p.Hkv;
+            if (sm.seq_len[b] != 0) continue;
+            for (int idx = threadIdx.x; idx < p.G * D; idx += kConsumerThreads)
+                p.out[(static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * p.G) * D + idx] = __float2bfloat16_rn(0.f);
+        }
+    }
+
+    int it = 0;
+    if (VAR == kSparse) {
+        Unit U;
+        U.u = sp_u;
+        U.b = sp_u / p.Hkv;
+        U.g = sp_u - U.b * p.Hkv;
+        U.len = p.width;
+        U.nt = 0;
+        U.base = 0;
+        cs.load_q(p, U.b, U.g);
+        cs.reset();
+        for (int t = t0; t < t1; ++t, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (it / S) & 1;
+            if (!mbar_wait(sm.full + s, ph, sm.abort, kWaitLimitNs)) {
+                *sm.abort = 1;
+                record_error(p.err, kErrWaitFull);
+                return;
+            }
+            const uint32_t ktile = smem_u32(sm.stages + s * Gm::kStageBytes);
+            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.empty + s);
+        }
+        finish_segment<D, GP>(p, sm, cs, U, p.nchunks == 1, blockIdx.x, sp_u * p.nchunks,
+                              p.nchunks, gphase);
+        return;
+    }
+
+    for (int t = t0; t < t1;) {
+        const Unit U = VAR == kDense ? locate_dense(p, t) : locate_paged(p, sm, t);
+        const int tend = min(t1, U.base + U.nt);
+        const bool whole = (t == U.base) && (tend == U.base + U.nt);
+        const int c_first = tile_owner(U.base, N, C);
+        const int c_last = tile_owner(U.base + U.nt - 1, N, C);
+        cs.load_q(p, U.b, U.g);
+        cs.reset();
+        for (; t < tend; ++t, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (it / S) & 1;
+            if (!mbar_wait(sm.full + s, ph, sm.abort, kWaitLimitNs)) {
+                *sm.abort = 1;
+                record_error(p.err, kErrWaitFull);
+                return;
+            }
+            const uint32_t ktile = smem_u32(sm.stages + s * Gm::kStageBytes);
+            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.empty + s);
+        }
+        if (!finish_segment<D, GP>(p, sm, cs, U, whole, static_cast<int>(blockIdx.x) + U.u,
+                                   c_first + U.u, c_last - c_first + 1, gphase))
+            return;
+    }
+}
+
+}  // namespace da

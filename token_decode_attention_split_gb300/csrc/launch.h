@@ -1,0 +1,32 @@
+// Internal launch interface between the C ABI (api.cu) and the per-variant kernel translation
+// units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "decode_kernel.cuh"
+
+namespace da {
+
+struct Launch {
+    CUtensorMap tm_k;   // unused by the sparse kernels
+    CUtensorMap tm_v;
+    Params p;
+    int grid;
+    cudaStream_t stream;
+};
+
+// Dynamic shared memory bytes of the kernel for head dim D and padded group GP (0 if none).
+int kernel_smem_bytes(int D, int GP);
+int kernel_stages(int D, int GP);
+
+cudaError_t launch_dense(int D, int GP, const Launch& L);
+cudaError_t launch_paged(int D, int GP, const Launch& L);
+cudaError_t launch_sparse(int D, int GP, const Launch& L);
+
+// Opts the kernel into `smem` bytes of dynamic shared memory on the current device (once per
+// kernel and device), then launches it.
+cudaError_t launch_kernel(const void* kernel, int smem, const Launch& L);
+
+}  // namespace da
