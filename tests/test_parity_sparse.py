@@ -48,7 +48,7 @@ def test_sparse_duplicates_interior_pads_and_bad_indices():
 
 
 def test_sparse_all_pad_rows_are_zero():
-    c = W.make_sparse(3, 8, 1, 128, 300, 400, 4, 0, seed=42, device=DEV)
+    c = W.make_sparse(3, 8, 1, 128, 1000, 400, 4, 0, seed=42, device=DEV)
     c.sel[1] = -1
     out = B_.run_case(c)
     got = out_f64(out)

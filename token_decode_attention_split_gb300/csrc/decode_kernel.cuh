@@ -399,6 +399,152 @@ __device__ __forceinline__ bool group_sync(const SmemPtrs& sm, uint32_t& phase, 
     return ok;
 }
 
+// Merges the nseg partial rows of unit U (workspace segments first_seg, first_seg + 1, ...) by
+// log-sum-exp, in segment order, and stores the bf16 output row of each of the G heads.  Runs on
+// the 128 consumer threads of the CTA that completed the unit and uses the merge area of shared
+// memory as scratch: the partial LSEs are read once, coalesced, into shared memory; each thread
+// then owns float4 slices of the output and keeps several partial rows in flight.
+template <int D, int GP>
+__device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, const Unit& U,
+                                           int first_seg, int nseg, uint32_t& gphase) {
+    using Gm = Geometry<D, GP>;
+    constexpr int D4 = D / 4;                        // float4 columns per row
+    constexpr int HQ = kConsumerThreads / D4;        // heads covered per pass (4 or 8)
+    constexpr int NH = (GP + HQ - 1) / HQ;           // heads per thread
+    constexpr int SU = NH >= 16 ? 1 : 16 / NH;       // segments whose rows are loaded together
+    constexpr int SB = Gm::KS * D - 4;               // segments per shared-memory batch
+    const int tid = threadIdx.x;
+    const int G = p.G;
+    float* h_max = sm.merge_o;                       // [GP]
+    float* h_inv = h_max + GP;                       // [GP]
+    int* h_live = reinterpret_cast<int*>(h_inv + GP);  // [GP]
+    int* h_only = h_live + GP;                       // [GP]
+    float* w_sm = reinterpret_cast<float*>(h_only + GP);  // [SB][GP]
+    const float* lse = p.part_lse + static_cast<size_t>(first_seg) * G;
+    const float4* orow = reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(first_seg) * G * D);
+    const bool one_batch = nseg <= SB;
+
+    if (!one_batch && tid < G) {
+        // many segments: per-head statistics straight from global memory
+        float M = -CUDART_INF_F;
+#pragma unroll 8
+        for (int k = 0; k < nseg; ++k) M = fmaxf(M, __ldcg(lse + static_cast<size_t>(k) * G + tid));
+        float L = 0.f;
+        int live = 0, only = 0;
+#pragma unroll 8
+        for (int k = 0; k < nseg; ++k) {
+            const float l = __ldcg(lse + static_cast<size_t>(k) * G + tid);
+            if (l != -CUDART_INF_F) {
+                const float w = fast_exp2(l - M);
+                L = live ? L + w : w;
+                ++live;
+                only = k;
+            }
+        }
+        h_max[tid] = M;
+        h_inv[tid] = live ? 1.0f / L : 0.f;
+        h_live[tid] = live;
+        h_only[tid] = only;
+    }
+
+    const int d4 = tid % D4, hq = tid / D4;
+    float4 acc[NH];
+    uint32_t started = 0;
+#pragma unroll
+    for (int j = 0; j < NH; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    for (int s0 = 0; s0 < nseg; s0 += SB) {
+        const int nb = min(SB, nseg - s0);
+        for (int i = tid; i < nb * G; i += kConsumerThreads) {
+            const int sgi = i / G, h = i - sgi * G;
+            w_sm[sgi * GP + h] = __ldcg(lse + static_cast<size_t>(s0 + sgi) * G + h);
+        }
+        if (!group_sync(sm, gphase, p.err)) return false;
+        if (one_batch) {
+            if (tid < G) {
+                float M = -CUDART_INF_F;
+                for (int k = 0; k < nb; ++k) M = fmaxf(M, w_sm[k * GP + tid]);
+                float L = 0.f;
+                int live = 0, only = 0;
+                for (int k = 0; k < nb; ++k) {
+                    const float l = w_sm[k * GP + tid];
+                    float w = 0.f;
+                    if (l != -CUDART_INF_F) {
+                        w = fast_exp2(l - M);
+                        L = live ? L + w : w;
+                        ++live;
+                        only = k;
+                    }
+                    w_sm[k * GP + tid] = w;
+                }
+                h_max[tid] = M;
+                h_inv[tid] = live ? 1.0f / L : 0.f;
+                h_live[tid] = live;
+                h_only[tid] = only;
+            }
+        } else {
+            for (int i = tid; i < nb * G; i += kConsumerThreads) {
+                const int sgi = i / G, h = i - sgi * G;
+                const float l = w_sm[sgi * GP + h];
+                w_sm[sgi * GP + h] = l == -CUDART_INF_F ? 0.f : fast_exp2(l - h_max[h]);
+            }
+        }
+        if (!group_sync(sm, gphase, p.err)) return false;
+        for (int sgi = 0; sgi < nb; sgi += SU) {
+            float w[SU][NH];
+            float4 o4[SU][NH];
+#pragma unroll
+            for (int u = 0; u < SU; ++u)
+#pragma unroll
+                for (int j = 0; j < NH; ++j) {
+                    const int h = hq + j * HQ;
+                    w[u][j] = (sgi + u < nb && h < G) ? w_sm[(sgi + u) * GP + h] : 0.f;
+                    o4[u][j] = w[u][j] != 0.f
+                                   ? __ldcg(orow + (static_cast<size_t>(s0 + sgi + u) * G + h) * D4 + d4)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+            for (int u = 0; u < SU; ++u)
+#pragma unroll
+                for (int j = 0; j < NH; ++j) {
+                    if (w[u][j] == 0.f) continue;
+                    const float ww = w[u][j];
+                    if (started & (1u << j)) {
+                        acc[j].x += ww * o4[u][j].x;
+                        acc[j].y += ww * o4[u][j].y;
+                        acc[j].z += ww * o4[u][j].z;
+                        acc[j].w += ww * o4[u][j].w;
+                    } else {
+                        acc[j] = make_float4(ww * o4[u][j].x, ww * o4[u][j].y, ww * o4[u][j].z,
+                                             ww * o4[u][j].w);
+                        started |= 1u << j;
+                    }
+                }
+        }
+        if (!group_sync(sm, gphase, p.err)) return false;
+    }
+
+    const size_t out_row0 = static_cast<size_t>(U.b) * p.Hq + static_cast<size_t>(U.g) * G;
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+        const int h = hq + j * HQ;
+        if (h >= G) continue;
+        const int live = h_live[h];
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live == 1) {
+            v = __ldcg(orow + (static_cast<size_t>(h_only[h]) * G + h) * D4 + d4);
+        } else if (live > 1) {
+            const float inv = h_inv[h];
+            v = make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv);
+        }
+        uint2 packed;
+        packed.x = pack_bf16x2(v.x, v.y);
+        packed.y = pack_bf16x2(v.z, v.w);
+        *reinterpret_cast<uint2*>(p.out + (out_row0 + h) * D + 4 * d4) = packed;
+    }
+    return true;
+}
+
 // Finishes one segment of unit U: merges the key-split warps, then either stores the output or
 // publishes a partial and, in the CTA that completes the unit, merges all partials.
 template <int D, int GP>
@@ -450,33 +596,7 @@ __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& 
         if (!group_sync(sm, gphase, p.err)) return false;
         if (*sm.last_flag) {
             __threadfence();
-            for (int idx = tid; idx < p.G * D; idx += kConsumerThreads) {
-                const int h = idx / D, d = idx - h * D;
-                float M = -CUDART_INF_F;
-                int live = 0, only = 0;
-                for (int k = 0; k < nseg; ++k) {
-                    const float l = __ldcg(p.part_lse + static_cast<size_t>(first_seg + k) * p.G + h);
-                    if (l != -CUDART_INF_F) { M = fmaxf(M, l); ++live; only = k; }
-                }
-                float val = 0.f;
-                if (live == 1) {
-                    val = __ldcg(p.part_o + (static_cast<size_t>(first_seg + only) * p.G + h) * D + d);
-                } else if (live > 1) {
-                    float L = 0.f, O = 0.f;
-                    bool first = true;
-                    for (int k = 0; k < nseg; ++k) {
-                        const size_t sk = static_cast<size_t>(first_seg + k);
-                        const float l = __ldcg(p.part_lse + sk * p.G + h);
-                        if (l == -CUDART_INF_F) continue;
-                        const float w = fast_exp2(l - M);
-                        const float ow = w * __ldcg(p.part_o + (sk * p.G + h) * D + d);
-                        if (first) { L = w; O = ow; first = false; }
-                        else { L += w; O += ow; }
-                    }
-                    val = O * (1.0f / L);
-                }
-                p.out[(out_row0 + h) * D + d] = __float2bfloat16_rn(val);
-            }
+            if (!merge_unit<D, GP>(p, sm, U, first_seg, nseg, gphase)) return false;
             if (tid == 0) p.counters[U.u] = 0u;
         }
     }
@@ -747,13 +867,16 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         return;
     }
 
+    Unit U;
+    if (t0 < t1) {
+        U = VAR == kDense ? locate_dense(p, t0) : locate_paged(p, sm, t0);
+        cs.load_q(p, U.b, U.g);
+    }
     for (int t = t0; t < t1;) {
-        const Unit U = VAR == kDense ? locate_dense(p, t) : locate_paged(p, sm, t);
         const int tend = min(t1, U.base + U.nt);
         const bool whole = (t == U.base) && (tend == U.base + U.nt);
         const int c_first = tile_owner(U.base, N, C);
         const int c_last = tile_owner(U.base + U.nt - 1, N, C);
-        cs.load_q(p, U.b, U.g);
         cs.reset();
         for (; t < tend; ++t, ++it) {
             const int s = it % S;
@@ -768,9 +891,16 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty + s);
         }
+        // the next segment's Q rows are fetched now so their latency hides behind the finish
+        Unit next = U;
+        if (t < t1) {
+            next = VAR == kDense ? locate_dense(p, t) : locate_paged(p, sm, t);
+            cs.load_q(p, next.b, next.g);
+        }
         if (!finish_segment<D, GP>(p, sm, cs, U, whole, static_cast<int>(blockIdx.x) + U.u,
                                    c_first + U.u, c_last - c_first + 1, gphase))
             return;
+        U = next;
     }
 }
 
