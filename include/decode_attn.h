@@ -135,6 +135,36 @@ da_status decode_attn_set_grid_limit(int max_ctas);
  * work, records a nonzero code here and returns instead of hanging; 0 means no such event. */
 da_status decode_attn_read_device_error(uint32_t *code);
 
+/* Bytes of the library-owned device scratch that decode_attn_dense_noalloc uses: 4 MiB, present
+ * on every GPU that loads the library until the process exits. */
+#define DECODE_ATTN_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+
+/*
+ * decode_attn_dense without a workspace argument, for callers that cannot allocate device memory
+ * where they call it: a plugin or custom operator inside a host framework that owns every device
+ * allocation and passes the operator only its inputs and outputs; code issuing work while a
+ * stream is being captured into a CUDA graph, where cudaMalloc is not allowed; latency-critical
+ * decode loops, where cudaMalloc may synchronise the device; processes that reserve nearly all
+ * HBM up front.  No counterpart in the pages: this entry point is an addition of this library.
+ *
+ * Same arguments, layouts and results as decode_attn_dense, minus the workspace: the scratch is a
+ * file-scope device array of DECODE_ATTN_NOALLOC_SCRATCH_BYTES bytes inside the library.
+ *   - Shapes whose workspace (decode_attn_workspace_size(DA_VARIANT_DENSE, ...)) exceeds that
+ *     size return DA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   - Every call shares the array: calls that can overlap on the GPU (different streams, or
+ *     several host threads on one device) race on it and must be serialised by the caller.
+ *   - Each call first clears, on `stream`, the part of the array it uses (the merge counters
+ *     must start at zero and the array keeps the previous call's contents); this clearing is the
+ *     only work it enqueues besides the kernel, and an argument error found after it leaves
+ *     nothing but the cleared scratch behind.
+ *   - The first call on each device looks up the array's device address (once, with that device
+ *     current) and caches it; make that first call before any stream capture on the device.
+ *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+da_status decode_attn_dense_noalloc(const void *q, const void *k, const void *v, void *out, int B,
+                                    int Hq, int Hkv, int D, int64_t capacity, int64_t k_len,
+                                    float softmax_scale, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,61 @@
+"""decode_attn_dense_noalloc, the dense entry point for callers that cannot allocate device
+memory (a framework-owned memory pool, a stream under graph capture, a latency-critical loop):
+it runs the same kernel with its workspace in a library-owned device array, so its output must
+match decode_attn_dense called with a caller-allocated workspace.  Kept in a file of its own that
+runs last."""
+import ctypes
+
+import pytest
+import torch
+
+from token_decode_attention_split_gb300 import binding as B_
+from token_decode_attention_split_gb300 import workloads as W
+
+from helpers import assert_close, out_f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+FAKE = 0x10000
+
+
+def noalloc_fn():
+    lib = B_.load_library()
+    fn = lib.decode_attn_dense_noalloc
+    vp, i, i64, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    fn.argtypes = [vp, vp, vp, vp, i, i, i, i, i64, i64, f, vp]
+    fn.restype = i
+    return fn
+
+
+def call_noalloc(fn, c, out, stream):
+    return fn(c.q.data_ptr(), c.k.data_ptr(), c.v.data_ptr(), out.data_ptr(), c.B, c.Hq, c.Hkv,
+              c.D, c.capacity, c.k_len, c.scale, stream.cuda_stream)
+
+
+@pytest.mark.parametrize("grid_limit", [0, 3])
+def test_noalloc_matches_workspace_entry_point(grid_limit):
+    """Two calls in a row through the C ABI, each compared with decode_attn_dense; with a grid
+    of 3 CTAs every head is merged from several partials, so the shared counters are exercised."""
+    fn = noalloc_fn()
+    B_.decode_attn_set_grid_limit(grid_limit)
+    try:
+        c = W.make_dense(2, 32, 4, 128, 3000, 2900, seed=77, device=DEV, k_scale=2.0,
+                         poison_tail=True)
+        ref = B_.run_case(c)
+        stream = torch.cuda.current_stream()
+        for _ in range(2):
+            out = torch.full(c.out_shape(), float("nan"), dtype=torch.bfloat16, device=DEV)
+            assert call_noalloc(fn, c, out, stream) == 0
+            torch.cuda.synchronize()
+            assert_close(out_f64(out), out_f64(ref), "noalloc vs workspace entry point")
+    finally:
+        B_.decode_attn_set_grid_limit(0)
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    fn = noalloc_fn()
+    need = B_.decode_attn_workspace_size(0, 1024, 64, 64, 128)
+    assert need > 4 * 1024 * 1024
+    status = fn(FAKE, FAKE, FAKE, FAKE, 1024, 64, 64, 128, 16, 8, 0.1, None)
+    assert status == 3    # DA_ERR_WORKSPACE_TOO_SMALL, nothing launched
+    assert B_.decode_attn_read_device_error() == 0
