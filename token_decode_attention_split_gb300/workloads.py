@@ -10,7 +10,8 @@ Recipe (every value comes from ``torch.Generator(...).manual_seed(seed)``):
   * dense: rows past ``k_len`` of K and V optionally set to NaN, so that reading them shows up.
   * paged: ``kv_len[b]`` uniform integers in [kv_min, kv_max]; the block table gives sequence b
     the consecutive slice ``perm[b*max_pages:(b+1)*max_pages]`` of one random permutation of the
-    page ids, so no two sequences share a page; every page no sequence uses, and every slot past
+    page ids (the identity with ``shuffle_pages=False``), so no two sequences share a page; every
+    page no sequence uses, and every slot past
     ``kv_len`` in a sequence's last page, is NaN.  The length buffer holds u32 words, either one
     per sequence (stride 1) or the ``{kv_len, q_offset, q_rope_pos}`` triple (stride 3).
   * sparse: each sequence's selection of ``width`` int32 entries is the ring-window slots
@@ -177,7 +178,7 @@ def make_dense(B, Hq, Hkv, D, capacity, k_len, seed, device="cpu", k_scale=1.0,
 
 def make_paged(B, Hq, Hkv, D, page_size, num_pages, kv_min, kv_max, seed, device="cpu",
                kv_len_stride=1, max_pages=None, kv_lens=None, poison_unused=True,
-               scale=None) -> PagedCase:
+               shuffle_pages=True, scale=None) -> PagedCase:
     dev, g, gc = _gens(seed, device)
     if kv_lens is None:
         kv_lens = torch.randint(kv_min, kv_max + 1, (B,), generator=gc).tolist()
@@ -187,6 +188,8 @@ def make_paged(B, Hq, Hkv, D, page_size, num_pages, kv_min, kv_max, seed, device
     if B * max_pages > num_pages:
         raise ValueError("pool too small for distinct pages per sequence")
     perm = torch.randperm(num_pages, generator=gc)
+    if not shuffle_pages:
+        perm = torch.arange(num_pages)   # sequence b owns pages [b*max_pages, (b+1)*max_pages)
     bt = perm[: B * max_pages].reshape(B, max_pages).to(torch.int32)
     q = _normal_bf16((B, Hq, 1, D), g, dev)
     k_pool = _normal_bf16((num_pages, Hkv, page_size, D), g, dev)
