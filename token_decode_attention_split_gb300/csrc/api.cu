@@ -90,6 +90,7 @@ struct WsLayout {
     size_t counters, lse, o, total;
 };
 
+// counters: one u32 per merge unit; lse: [segments][G]; o: [segments][G][D] (G = heads per segment)
 WsLayout ws_layout(long long units, long long segments, int G, int D) {
     WsLayout w;
     w.counters = 0;
@@ -121,6 +122,7 @@ Params base_params(const void* q, void* out, int B, int Hq, int Hkv, float scale
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.G = Hq / Hkv;
+    p.seg_heads = p.G;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = err;
     return p;
@@ -151,6 +153,24 @@ bool encode_3d(CUtensorMap* map, const void* base, cuuint64_t d0, cuuint64_t d1,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One page of one KV head ([page_size rows][D]) as a single box: dims (64 columns, rows, the two
+// 64-column halves, page-heads); the halves dimension has a 128-byte stride inside each 256-byte
+// row, so one box carries both halves, written to shared memory one half after the other.
+bool encode_page_4d(CUtensorMap* map, const void* base, int page_size, int Hkv, int64_t num_pages,
+                    cuuint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t row_bytes = 256;   // D = 128
+    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(page_size), 2,
+                                static_cast<cuuint64_t>(num_pages) * Hkv};
+    const cuuint64_t strides[3] = {row_bytes, 128, row_bytes * page_size};
+    const cuuint32_t box[4] = {64, box_rows, 2, 1};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // CTAs for a persistent dense/paged launch on `dev`.
 int persistent_ctas(int dev) {
     const int sms = sm_count(dev);
@@ -158,7 +178,13 @@ int persistent_ctas(int dev) {
     return (lim > 0 && lim < sms) ? lim : sms;
 }
 
-long long sparse_chunks(long long width) { return (width + kSparseChunkKeys - 1) / kSparseChunkKeys; }
+// Sparse work split: query-head groups of 16 when G > 16, and chunks of 512 selection entries
+// per head group.  Both depend on G only, never on the width, B or the device.
+int sparse_head_groups(int G) { return G <= kSparseHeadGroup ? 1 : (G + kSparseHeadGroup - 1) / kSparseHeadGroup; }
+int sparse_segment_heads(int G) { return G <= kSparseHeadGroup ? G : kSparseHeadGroup; }
+int sparse_padded_group(int G) { return G <= 8 ? 8 : 16; }
+long long sparse_chunk_keys(int G) { return static_cast<long long>(kSparseChunkUnit) * sparse_head_groups(G); }
+long long sparse_chunks(long long width, int G) { return (width + sparse_chunk_keys(G) - 1) / sparse_chunk_keys(G); }
 
 }  // namespace
 
@@ -196,8 +222,19 @@ cudaError_t launch_kernel(const void* kernel, int smem, const Launch& L) {
     }
     void* args[] = {const_cast<CUtensorMap*>(&L.tm_k), const_cast<CUtensorMap*>(&L.tm_v),
                     const_cast<Params*>(&L.p)};
-    return cudaLaunchKernel(kernel, dim3(L.grid), dim3(kThreads), args, static_cast<size_t>(smem),
-                            L.stream);
+    // Programmatic stream serialization: the kernel may be scheduled while the previous kernel
+    // in the stream drains; it waits for that kernel's completion before touching memory.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = L.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, kernel, args);
 }
 
 }  // namespace da
@@ -233,7 +270,8 @@ size_t decode_attn_workspace_size(int variant, int B, int Hq, int Hkv, int D, in
         segments = units + sms;
     } else if (variant == DA_VARIANT_SPARSE) {
         if (max_kv < 0) return 0;
-        segments = units * sparse_chunks(max_kv);
+        const long long groups = units * sparse_head_groups(G);
+        return ws_layout(groups, groups * sparse_chunks(max_kv, G), sparse_segment_heads(G), D).total;
     } else {
         return 0;
     }
@@ -339,10 +377,18 @@ da_status decode_attn_paged(const void* q, const void* k_pool, const void* v_poo
     const cuuint64_t row_bytes = static_cast<cuuint64_t>(D) * 2;
     const cuuint64_t page_bytes = row_bytes * page_size * Hkv;
     const cuuint32_t box_rows = static_cast<cuuint32_t>(std::min(page_size, kTileKeys));
-    if (!encode_3d(&L.tm_k, k_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
-                   row_bytes, page_bytes, box_rows) ||
-        !encode_3d(&L.tm_v, v_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
-                   row_bytes, page_bytes, box_rows))
+    // D = 128: one box per page and tensor when the driver accepts the 4-D descriptor; else (and
+    // for D = 64, whose page is a single 128-byte-wide box anyway) one 3-D box per half.
+    int box_4d = 0;
+    if (D == 128 && static_cast<long long>(num_pages) * Hkv < (1ll << 31) &&
+        encode_page_4d(&L.tm_k, k_pool, page_size, Hkv, num_pages, box_rows) &&
+        encode_page_4d(&L.tm_v, v_pool, page_size, Hkv, num_pages, box_rows))
+        box_4d = 1;
+    if (!box_4d &&
+        (!encode_3d(&L.tm_k, k_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
+                    row_bytes, page_bytes, box_rows) ||
+         !encode_3d(&L.tm_v, v_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
+                    row_bytes, page_bytes, box_rows)))
         return DA_ERR_CUDA;
     L.p = base_params(q, out, B, Hq, Hkv, softmax_scale, device_error_ptr(dev));
     bind_workspace(L.p, workspace, w);
@@ -352,6 +398,7 @@ da_status decode_attn_paged(const void* q, const void* k_pool, const void* v_poo
     L.p.num_pages = static_cast<int>(num_pages);
     L.p.kv_lens = kv_lens;
     L.p.kv_stride = kv_len_stride;
+    L.p.page_box_4d = box_4d;
     L.grid = persistent_ctas(dev);
     L.stream = cs;
     return launch_paged(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
@@ -368,14 +415,16 @@ da_status decode_attn_sparse(const void* q, const void* k_pool, const void* v_po
     if (width > 0 && (!sel || !aligned(sel, 4))) return DA_ERR_INVALID_ARGUMENT;
     if (pool_rows >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
     const long long units = static_cast<long long>(B) * Hkv;
-    const long long chunks = sparse_chunks(width);
-    if (units * chunks >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
+    const int G = Hq / Hkv;
+    const long long groups = units * sparse_head_groups(G);
+    const long long chunks = sparse_chunks(width, G);
+    if (groups * chunks >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (B == 0) return DA_OK;
     const int dev = current_device();
     if (dev < 0) return DA_ERR_CUDA;
-    const int G = Hq / Hkv, GP = padded_group(G);
-    const WsLayout w = ws_layout(units, units * chunks, G, D);
+    const int GP = sparse_padded_group(G);
+    const WsLayout w = ws_layout(groups, groups * chunks, sparse_segment_heads(G), D);
     if (workspace_bytes < w.total) return DA_ERR_WORKSPACE_TOO_SMALL;
     if (width == 0) return zero_output(out, B, Hq, D, cs);
 
@@ -386,9 +435,12 @@ da_status decode_attn_sparse(const void* q, const void* k_pool, const void* v_po
     L.p.width = width;
     L.p.pool_rows = static_cast<int>(pool_rows);
     L.p.nchunks = static_cast<int>(chunks);
+    L.p.nhg = sparse_head_groups(G);
+    L.p.chunk_keys = static_cast<int>(sparse_chunk_keys(G));
+    L.p.seg_heads = sparse_segment_heads(G);
     L.p.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
     L.p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
-    L.grid = static_cast<int>(units * chunks);
+    L.grid = static_cast<int>(groups * chunks);
     L.stream = cs;
     return launch_sparse(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }

@@ -4,9 +4,10 @@
 // processed together so every K/V row is read from HBM exactly once.  A unit's live rows are cut
 // into 64-row tiles.  Dense and paged calls run a persistent grid (one CTA per SM): the tiles of
 // all units are laid end to end and CTA c takes the contiguous range [c*N/C, (c+1)*N/C), so the
-// load is balanced to one tile whatever the lengths.  Sparse calls give each CTA one fixed
-// 256-entry chunk of one unit's selection (fixed so that trailing -1 pads cannot move a chunk
-// boundary).  Each CTA's piece of a unit is a "segment".
+// load is balanced to one tile whatever the lengths.  Sparse calls give each CTA up to 16 query
+// heads of one unit over one chunk of 512 * ceil(G / 16) selection entries: the chunk depends on
+// G only, so trailing -1 pads cannot move a chunk boundary, and the usual top-k width of a few
+// thousand entries needs no merge.  Each CTA's piece of a unit is a "segment".
 //
 // Inside a CTA.  Warp 4 is the producer: it streams K and V tiles into a ring of shared-memory
 // stages (TMA tile loads with 128-byte swizzle for dense and paged; cp.async 16-byte gathers with
@@ -19,6 +20,10 @@
 // its normalised partial row and log2-sum-exp to the workspace and bumps the unit's counter; the
 // CTA that completes the unit merges all its partials by log-sum-exp in segment order (so the
 // result does not depend on which CTA finishes last) and resets the counter to zero.
+//
+// Launch.  Kernels are launched with programmatic stream serialization: a CTA sets up its shared
+// memory while the previous kernel in the stream drains, then waits for that kernel's completion
+// (griddepcontrol.wait) before its first global-memory access.
 //
 // Safety.  Every wait is bounded (about one second); on timeout the CTA records an error code in
 // the device error word, waits for its own copies in flight and returns.
@@ -39,8 +44,8 @@ constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr int kSparseChunkKeys = 256;
-constexpr int kSparseChunkTiles = kSparseChunkKeys / kTileKeys;
+constexpr int kSparseHeadGroup = 16;         // query heads per CTA when a group is split
+constexpr int kSparseChunkUnit = 512;         // sparse chunk = 512 entries per head group
 constexpr int kMaxPagedBatch = 1024;
 constexpr int kSmemBudget = 232448;           // opt-in dynamic shared memory per block
 
@@ -76,9 +81,10 @@ struct Params {
     __nv_bfloat16* out;       // [B, Hq, D]
     int B, Hq, Hkv, G;
     float scale_log2;         // softmax_scale * log2(e)
-    unsigned* counters;       // [B * Hkv] segment counters, zero between calls
-    float* part_o;            // [segments, G, D]
-    float* part_lse;          // [segments, G] (log2 domain)
+    unsigned* counters;       // one per merge unit, zero between calls
+    float* part_o;            // [segments, seg_heads, D]
+    float* part_lse;          // [segments, seg_heads] (log2 domain)
+    int seg_heads;            // heads per segment: G, or the head-group size for sparse
     unsigned* err;            // device error word
     // dense
     int k_len;
@@ -86,11 +92,14 @@ struct Params {
     // paged
     const int* block_table;
     int max_pages, page_size, num_pages;
+    int page_box_4d;          // 1: one 4-D box per page (both halves), 0: one 3-D box per half
     const unsigned* kv_lens;
     int kv_stride;
     // sparse
     const int* sel;
     int width, pool_rows, nchunks;
+    int nhg;                  // head groups per KV head (sparse)
+    int chunk_keys;           // selection entries per chunk (sparse), a multiple of 64
     const __nv_bfloat16* k_pool;
     const __nv_bfloat16* v_pool;
 };
@@ -100,6 +109,9 @@ struct Unit {
     int len;    // live rows
     int nt;     // tiles
     int base;   // global index of the unit's first tile
+    int hq0;    // q / out row of the first query head this CTA handles
+    int nh;     // query heads this CTA handles
+    int cu;     // merge counter of this (unit, head group)
 };
 
 struct SmemPtrs {
@@ -146,11 +158,17 @@ __device__ __forceinline__ void record_error(unsigned* err, unsigned code) {
     if (err) atomicCAS(err, 0u, code);
 }
 
-// Byte offset, inside one K or V tile, of 16-byte chunk c (of D/8) of row r.  Each 64-column
-// half of the tile is [64 rows][128 B] with chunk index XOR (row & 7): the layout a TMA tile load
-// with 128-byte swizzle produces, and the one the sparse gather writes by hand.
-__device__ __forceinline__ uint32_t tile_offset(int r, int c) {
-    return static_cast<uint32_t>((c >> 3) * (kTileKeys * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// Byte offset, inside one K or V tile, of 16-byte chunk c (of D/8) of row r.  The tile is cut
+// into blocks of 2^rb_shift rows (64 for dense and sparse, one page for paged); a block holds its
+// 64-column halves one after the other, each [rows][128 B] with the 16-byte chunk index XOR
+// (row & 7).  That is the layout a TMA tile load with 128-byte swizzle writes for one block, and
+// the one the sparse gather writes by hand.
+template <int HALVES>
+__device__ __forceinline__ uint32_t tile_offset(int r, int c, int rb_shift) {
+    const int blk = r >> rb_shift;
+    const int rr = r & ((1 << rb_shift) - 1);
+    return static_cast<uint32_t>(((blk * HALVES + (c >> 3)) << (rb_shift + 7)) + rr * 128 +
+                                 (((c & 7) ^ (r & 7)) << 4));
 }
 
 // ------------------------------------------------------------------ schedule
@@ -174,6 +192,9 @@ __device__ __forceinline__ Unit locate_dense(const Params& p, int t) {
     U.g = U.u - U.b * p.Hkv;
     U.len = p.k_len;
     U.base = U.u * U.nt;
+    U.hq0 = U.b * p.Hq + U.g * p.G;
+    U.nh = p.G;
+    U.cu = U.u;
     return U;
 }
 
@@ -192,6 +213,9 @@ __device__ __forceinline__ Unit locate_paged(const Params& p, const SmemPtrs& sm
     U.u = U.b * p.Hkv + U.g;
     U.len = sm.seq_len[lo];
     U.base = sm.seq_prefix[lo] * p.Hkv + U.g * U.nt;
+    U.hq0 = U.b * p.Hq + U.g * p.G;
+    U.nh = p.G;
+    U.cu = U.u;
     return U;
 }
 
@@ -217,13 +241,13 @@ struct ConsumerState {
         return hg * Gm::NT * 8 + nt * 8 + 2 * qd + hc;
     }
 
-    __device__ __forceinline__ void load_q(const Params& p, int b, int g) {
+    // Q rows hq0 .. hq0 + nh - 1 as B fragments (heads past nh are zero)
+    __device__ __forceinline__ void load_q(const Params& p, int hq0, int nh) {
 #pragma unroll
         for (int nt = 0; nt < Gm::NT; ++nt) {
             const int head = hg * Gm::NT * 8 + nt * 8 + gq;
-            const bool ok = head < p.G;
-            const __nv_bfloat16* row =
-                p.q + (static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * p.G + (ok ? head : 0)) * D;
+            const bool ok = head < nh;
+            const __nv_bfloat16* row = p.q + (static_cast<size_t>(hq0) + (ok ? head : 0)) * D;
             const uint32_t* row32 = reinterpret_cast<const uint32_t*>(row);
 #pragma unroll
             for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
@@ -249,7 +273,7 @@ struct ConsumerState {
 
     // One stage: this warp's MT*16 rows of the tile.  `mask` bit r = row r of the tile is valid.
     __device__ __forceinline__ void consume(uint32_t k_tile, uint32_t v_tile, uint64_t mask,
-                                            float scale_log2) {
+                                            float scale_log2, int rb_shift) {
         constexpr int kRows = Gm::MT * 16;
         const uint64_t rows_mask = kRows == 64 ? ~0ull : ((1ull << kRows) - 1ull);
         const uint64_t wmask = (mask >> (kg * kRows)) & rows_mask;
@@ -271,7 +295,7 @@ struct ConsumerState {
 #pragma unroll
             for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
                 uint32_t a[4];
-                ldmatrix_x4(a, k_tile + tile_offset(r, 2 * ks + (lane >> 4)));
+                ldmatrix_x4(a, k_tile + tile_offset<Gm::kHalves>(r, 2 * ks + (lane >> 4), rb_shift));
 #pragma unroll
                 for (int nt = 0; nt < Gm::NT; ++nt) mma_bf16_16816(s[mt][nt], a, qf[ks][nt][0], qf[ks][nt][1]);
             }
@@ -349,7 +373,7 @@ struct ConsumerState {
 #pragma unroll
             for (int dt = 0; dt < Gm::DT; ++dt) {
                 uint32_t a[4];
-                ldmatrix_x4_trans(a, v_tile + tile_offset(r, 2 * dt + ((lane >> 3) & 1)));
+                ldmatrix_x4_trans(a, v_tile + tile_offset<Gm::kHalves>(r, 2 * dt + ((lane >> 3) & 1), rb_shift));
                 if (!all_valid) {   // rows never loaded or past the length may hold NaN
                     a[0] &= keep_lo;
                     a[1] &= keep_lo;
@@ -414,26 +438,27 @@ __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, 
     constexpr int SU = NH >= 16 ? 1 : 16 / NH;       // segments whose rows are loaded together
     constexpr int SB = Gm::KS * D - 4;               // segments per shared-memory batch
     const int tid = threadIdx.x;
-    const int G = p.G;
+    const int G = U.nh;                              // heads of this unit
+    const int SH = p.seg_heads;                      // partial-row stride per segment
     float* h_max = sm.merge_o;                       // [GP]
     float* h_inv = h_max + GP;                       // [GP]
     int* h_live = reinterpret_cast<int*>(h_inv + GP);  // [GP]
     int* h_only = h_live + GP;                       // [GP]
     float* w_sm = reinterpret_cast<float*>(h_only + GP);  // [SB][GP]
-    const float* lse = p.part_lse + static_cast<size_t>(first_seg) * G;
-    const float4* orow = reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(first_seg) * G * D);
+    const float* lse = p.part_lse + static_cast<size_t>(first_seg) * SH;
+    const float4* orow = reinterpret_cast<const float4*>(p.part_o + static_cast<size_t>(first_seg) * SH * D);
     const bool one_batch = nseg <= SB;
 
     if (!one_batch && tid < G) {
         // many segments: per-head statistics straight from global memory
         float M = -CUDART_INF_F;
 #pragma unroll 8
-        for (int k = 0; k < nseg; ++k) M = fmaxf(M, __ldcg(lse + static_cast<size_t>(k) * G + tid));
+        for (int k = 0; k < nseg; ++k) M = fmaxf(M, __ldcg(lse + static_cast<size_t>(k) * SH + tid));
         float L = 0.f;
         int live = 0, only = 0;
 #pragma unroll 8
         for (int k = 0; k < nseg; ++k) {
-            const float l = __ldcg(lse + static_cast<size_t>(k) * G + tid);
+            const float l = __ldcg(lse + static_cast<size_t>(k) * SH + tid);
             if (l != -CUDART_INF_F) {
                 const float w = fast_exp2(l - M);
                 L = live ? L + w : w;
@@ -457,7 +482,7 @@ __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, 
         const int nb = min(SB, nseg - s0);
         for (int i = tid; i < nb * G; i += kConsumerThreads) {
             const int sgi = i / G, h = i - sgi * G;
-            w_sm[sgi * GP + h] = __ldcg(lse + static_cast<size_t>(s0 + sgi) * G + h);
+            w_sm[sgi * GP + h] = __ldcg(lse + static_cast<size_t>(s0 + sgi) * SH + h);
         }
         if (!group_sync(sm, gphase, p.err)) return false;
         if (one_batch) {
@@ -500,7 +525,7 @@ __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, 
                     const int h = hq + j * HQ;
                     w[u][j] = (sgi + u < nb && h < G) ? w_sm[(sgi + u) * GP + h] : 0.f;
                     o4[u][j] = w[u][j] != 0.f
-                                   ? __ldcg(orow + (static_cast<size_t>(s0 + sgi + u) * G + h) * D4 + d4)
+                                   ? __ldcg(orow + (static_cast<size_t>(s0 + sgi + u) * SH + h) * D4 + d4)
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
@@ -524,7 +549,7 @@ __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, 
         if (!group_sync(sm, gphase, p.err)) return false;
     }
 
-    const size_t out_row0 = static_cast<size_t>(U.b) * p.Hq + static_cast<size_t>(U.g) * G;
+    const size_t out_row0 = static_cast<size_t>(U.hq0);
 #pragma unroll
     for (int j = 0; j < NH; ++j) {
         const int h = hq + j * HQ;
@@ -532,7 +557,7 @@ __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, 
         const int live = h_live[h];
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (live == 1) {
-            v = __ldcg(orow + (static_cast<size_t>(h_only[h]) * G + h) * D4 + d4);
+            v = __ldcg(orow + (static_cast<size_t>(h_only[h]) * SH + h) * D4 + d4);
         } else if (live > 1) {
             const float inv = h_inv[h];
             v = make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv);
@@ -557,8 +582,9 @@ __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& 
     cs.stash(sm);
     if (!group_sync(sm, gphase, p.err)) return false;
 
-    const size_t out_row0 = (static_cast<size_t>(U.b) * p.Hq + static_cast<size_t>(U.g) * p.G);
-    for (int idx = tid; idx < p.G * D; idx += kConsumerThreads) {
+    const size_t out_row0 = static_cast<size_t>(U.hq0);
+    const size_t SH = static_cast<size_t>(p.seg_heads);
+    for (int idx = tid; idx < U.nh * D; idx += kConsumerThreads) {
         const int h = idx / D, d = idx - h * D;
         float M = -CUDART_INF_F;
 #pragma unroll
@@ -582,22 +608,22 @@ __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& 
         if (whole) {
             p.out[(out_row0 + h) * D + d] = __float2bfloat16_rn(val);
         } else {
-            p.part_o[(static_cast<size_t>(seg) * p.G + h) * D + d] = val;
-            if (d == 0) p.part_lse[static_cast<size_t>(seg) * p.G + h] = empty ? -CUDART_INF_F : M + fast_log2(L);
+            p.part_o[(static_cast<size_t>(seg) * SH + h) * D + d] = val;
+            if (d == 0) p.part_lse[static_cast<size_t>(seg) * SH + h] = empty ? -CUDART_INF_F : M + fast_log2(L);
         }
     }
     if (!whole) {
         __threadfence();
         if (!group_sync(sm, gphase, p.err)) return false;
         if (tid == 0) {
-            const unsigned prev = atomicAdd(p.counters + U.u, 1u);
+            const unsigned prev = atomicAdd(p.counters + U.cu, 1u);
             *sm.last_flag = (prev == static_cast<unsigned>(nseg - 1)) ? 1 : 0;
         }
         if (!group_sync(sm, gphase, p.err)) return false;
         if (*sm.last_flag) {
             __threadfence();
             if (!merge_unit<D, GP>(p, sm, U, first_seg, nseg, gphase)) return false;
-            if (tid == 0) p.counters[U.u] = 0u;
+            if (tid == 0) p.counters[U.cu] = 0u;
         }
     }
     return group_sync(sm, gphase, p.err);
@@ -628,6 +654,11 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
     }
+    // Everything above touches only shared memory and the kernel parameters, so it overlaps the
+    // tail of the previous kernel in the stream; no global memory is read or written before the
+    // previous kernels have completed.
+    grid_dependency_wait();
+    allow_dependent_launch();
 
     // ---- schedule
     int N = 0, C = 1, t0 = 0, t1 = 0;
@@ -669,14 +700,17 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         t0 = static_cast<int>(static_cast<long long>(blockIdx.x) * N / C);
         t1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * N / C);
     }
-    // sparse: this CTA's chunk of one unit
-    int sp_u = 0, sp_chunk = 0;
+    // sparse: this CTA's chunk of one (unit, head group); blockIdx.x = (u * nhg + hg) * nchunks + chunk
+    int sp_u = 0, sp_cu = 0, sp_hg = 0, sp_key0 = 0, sp_nkeys = 0;
     if (VAR == kSparse) {
-        sp_u = blockIdx.x / p.nchunks;
-        sp_chunk = blockIdx.x - sp_u * p.nchunks;
-        const int ntiles = (p.width + kTileKeys - 1) / kTileKeys;
-        t0 = sp_chunk * kSparseChunkTiles;
-        t1 = min(t0 + kSparseChunkTiles, ntiles);
+        sp_cu = blockIdx.x / p.nchunks;
+        const int chunk = blockIdx.x - sp_cu * p.nchunks;
+        sp_u = sp_cu / p.nhg;
+        sp_hg = sp_cu - sp_u * p.nhg;
+        sp_key0 = chunk * p.chunk_keys;
+        sp_nkeys = min(p.chunk_keys, p.width - sp_key0);
+        t0 = sp_key0 / kTileKeys;
+        t1 = (sp_key0 + sp_nkeys + kTileKeys - 1) / kTileKeys;
     }
 
     if (warp == kConsumerWarps) {
@@ -692,17 +726,25 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             const bool isv = w >= CH;
             const int c = isv ? w - CH : w;
             const __nv_bfloat16* pool = isv ? p.v_pool : p.k_pool;
-            const int* selrow = p.sel + static_cast<size_t>(b) * p.width;
+            // this chunk's entries, read once (coalesced, all in flight) into shared memory with
+            // every entry outside [0, pool_rows) folded to -1
+            int* sidx = sm.seq_prefix;
+            const int* selrow = p.sel + static_cast<size_t>(b) * p.width + sp_key0;
+            for (int i = lane; i < sp_nkeys; i += 32) {
+                const int idx = __ldg(selrow + i);
+                sidx[i] = (idx >= 0 && idx < p.pool_rows) ? idx : -1;
+            }
+            __syncwarp();
             for (int t = t0; t < t1 && ok; ++t, ++it) {
                 const int s = it % S;
                 const uint32_t ph = (it / S) & 1;
                 if (!mbar_wait(sm.empty + s, ph ^ 1u, sm.abort, kWaitLimitNs)) { ok = false; break; }
-                const int key0 = t * kTileKeys;
-                const int i0 = key0 + lane, i1 = key0 + 32 + lane;
-                const int idx0 = i0 < p.width ? __ldg(selrow + i0) : -1;
-                const int idx1 = i1 < p.width ? __ldg(selrow + i1) : -1;
-                const bool v0 = idx0 >= 0 && idx0 < p.pool_rows;
-                const bool v1 = idx1 >= 0 && idx1 < p.pool_rows;
+                const int l0 = t * kTileKeys - sp_key0;
+                const int i0 = l0 + lane, i1 = l0 + 32 + lane;
+                const int idx0 = i0 < sp_nkeys ? sidx[i0] : -1;
+                const int idx1 = i1 < sp_nkeys ? sidx[i1] : -1;
+                const bool v0 = idx0 >= 0;
+                const bool v1 = idx1 >= 0;
                 const uint64_t mask = static_cast<uint64_t>(__ballot_sync(0xffffffffu, v0)) |
                                       (static_cast<uint64_t>(__ballot_sync(0xffffffffu, v1)) << 32);
                 unsigned char* tile = sm.stages + s * Gm::kStageBytes + (isv ? Gm::kTileBytes : 0);
@@ -713,7 +755,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     const bool valid = (mask >> r) & 1ull;
                     const __nv_bfloat16* src =
                         pool + (static_cast<size_t>(sp_u) * p.pool_rows + (valid ? idx : 0)) * D + c * 8;
-                    cp_async_16(tile + tile_offset(r, c), src, valid ? 16u : 0u);
+                    cp_async_16(tile + tile_offset<Gm::kHalves>(r, c, 6), src, valid ? 16u : 0u);
                 }
                 if (lane == 0) sm.stage_mask[s] = mask;
                 cp_async_arrive_noinc(sm.full + s);
@@ -793,11 +835,19 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                             mbar_arrive_expect_tx(sm.full + s, nloaded * 2u * Gm::kHalves * box_bytes);
                             for (int i = 0; i < pages_per_tile; ++i) {
                                 if (!(page_ok & (1u << i))) continue;
+                                // block i of the tile: its halves one after the other
+                                const int dst = i * Gm::kHalves * box_rows * 128;
+                                if (p.page_box_4d) {
+                                    const int ph = pages[i] * p.Hkv + U.g;
+                                    tma_load_4d(ktile + dst, &tm_k, 0, row_in_page, 0, ph, sm.full + s);
+                                    tma_load_4d(vtile + dst, &tm_v, 0, row_in_page, 0, ph, sm.full + s);
+                                } else {
 #pragma unroll
-                                for (int h = 0; h < Gm::kHalves; ++h) {
-                                    const int dst = h * kTileKeys * 128 + i * box_rows * 128;
-                                    tma_load_3d(ktile + dst, &tm_k, 64 * h, U.g * P + row_in_page, pages[i], sm.full + s);
-                                    tma_load_3d(vtile + dst, &tm_v, 64 * h, U.g * P + row_in_page, pages[i], sm.full + s);
+                                    for (int h = 0; h < Gm::kHalves; ++h) {
+                                        const int dh = dst + h * box_rows * 128;
+                                        tma_load_3d(ktile + dh, &tm_k, 64 * h, U.g * P + row_in_page, pages[i], sm.full + s);
+                                        tma_load_3d(vtile + dh, &tm_v, 64 * h, U.g * P + row_in_page, pages[i], sm.full + s);
+                                    }
                                 }
                             }
                         }
@@ -823,6 +873,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
 
     // ==================================================================== consumer warps
+    const int rb_shift = VAR == kPaged ? 31 - __clz(min(p.page_size, kTileKeys)) : 6;
     ConsumerState<D, GP> cs;
     cs.init(warp, lane);
     uint32_t gphase = 0;
@@ -847,7 +898,11 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         U.len = p.width;
         U.nt = 0;
         U.base = 0;
-        cs.load_q(p, U.b, U.g);
+        const int hgs = p.nhg > 1 ? kSparseHeadGroup : p.G;
+        U.hq0 = U.b * p.Hq + U.g * p.G + sp_hg * hgs;
+        U.nh = min(hgs, p.G - sp_hg * hgs);
+        U.cu = sp_cu;
+        cs.load_q(p, U.hq0, U.nh);
         cs.reset();
         for (int t = t0; t < t1; ++t, ++it) {
             const int s = it % S;
@@ -858,11 +913,11 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 return;
             }
             const uint32_t ktile = smem_u32(sm.stages + s * Gm::kStageBytes);
-            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2);
+            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2, rb_shift);
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty + s);
         }
-        finish_segment<D, GP>(p, sm, cs, U, p.nchunks == 1, blockIdx.x, sp_u * p.nchunks,
+        finish_segment<D, GP>(p, sm, cs, U, p.nchunks == 1, blockIdx.x, sp_cu * p.nchunks,
                               p.nchunks, gphase);
         return;
     }
@@ -870,7 +925,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     Unit U;
     if (t0 < t1) {
         U = VAR == kDense ? locate_dense(p, t0) : locate_paged(p, sm, t0);
-        cs.load_q(p, U.b, U.g);
+        cs.load_q(p, U.hq0, U.nh);
     }
     for (int t = t0; t < t1;) {
         const int tend = min(t1, U.base + U.nt);
@@ -887,7 +942,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 return;
             }
             const uint32_t ktile = smem_u32(sm.stages + s * Gm::kStageBytes);
-            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2);
+            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2, rb_shift);
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty + s);
         }
@@ -895,7 +950,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         Unit next = U;
         if (t < t1) {
             next = VAR == kDense ? locate_dense(p, t) : locate_paged(p, sm, t);
-            cs.load_q(p, next.b, next.g);
+            cs.load_q(p, next.hq0, next.nh);
         }
         if (!finish_segment<D, GP>(p, sm, cs, U, whole, static_cast<int>(blockIdx.x) + U.u,
                                    c_first + U.u, c_last - c_first + 1, gphase))

@@ -1,4 +1,5 @@
-// sparse decode-attention kernel instantiations (head dim 64/128, padded group 8/16/32/64).
+// sparse decode-attention kernel instantiations (head dim 64/128; a CTA takes at most 16
+// query heads, so only the padded groups 8 and 16 exist).
 #include "launch.h"
 
 namespace da {
@@ -14,15 +15,11 @@ cudaError_t launch_sparse(int D, int GP, const Launch& L) {
         switch (GP) {
             case 8: return run_sparse<64, 8>(L);
             case 16: return run_sparse<64, 16>(L);
-            case 32: return run_sparse<64, 32>(L);
-            case 64: return run_sparse<64, 64>(L);
         }
     } else if (D == 128) {
         switch (GP) {
             case 8: return run_sparse<128, 8>(L);
             case 16: return run_sparse<128, 16>(L);
-            case 32: return run_sparse<128, 32>(L);
-            case 64: return run_sparse<128, 64>(L);
         }
     }
     return cudaErrorInvalidValue;
