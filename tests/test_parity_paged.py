@@ -29,6 +29,8 @@ CASES = [
     (2, 64, 8, 128, 128, 64, 100, 900, 1),
     (2, 16, 16, 128, 256, 32, 200, 1000, 3),
     (3, 64, 1, 128, 16, 300, 1, 800, 1),
+    (3, 32, 8, 128, 8, 2048, 1, 700, 1),    # 8-row pages: four KV heads per unit
+    (2, 24, 8, 64, 16, 600, 5, 900, 3),     # G = 3, D = 64: four KV heads per unit
 ]
 
 

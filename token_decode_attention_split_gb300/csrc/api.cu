@@ -123,6 +123,8 @@ Params base_params(const void* q, void* out, int B, int Hq, int Hkv, float scale
     p.Hkv = Hkv;
     p.G = Hq / Hkv;
     p.seg_heads = p.G;
+    p.kh = 1;
+    p.tile_keys = kTileKeys;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = err;
     return p;
@@ -153,20 +155,34 @@ bool encode_3d(CUtensorMap* map, const void* base, cuuint64_t d0, cuuint64_t d1,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// One page of one KV head ([page_size rows][D]) as a single box: dims (64 columns, rows, the two
-// 64-column halves, page-heads); the halves dimension has a 128-byte stride inside each 256-byte
-// row, so one box carries both halves, written to shared memory one half after the other.
-bool encode_page_4d(CUtensorMap* map, const void* base, int page_size, int Hkv, int64_t num_pages,
-                    cuuint32_t box_rows) {
+// KV heads per paged unit: the smallest power of two that makes one page of those heads at least
+// 8 KB (a TMA box that size streams at full rate; a 4 KB one does not), limited so the unit's
+// query heads fit one CTA (kh * G <= 64), kh divides Hkv, and a stage keeps >= 8 keys per head.
+int paged_kv_heads(int Hkv, int G, int page_size, int D) {
+    int kh = 1;
+    while (kh < 8 && static_cast<long long>(kh) * page_size * D * 2 < 8192 && Hkv % (2 * kh) == 0 &&
+           2 * kh * G <= 64)
+        kh *= 2;
+    return kh;
+}
+
+// One page of kh adjacent KV heads as a single box: dims (64 columns, rows of a page, the
+// 64-column halves, KV heads, pages).  The halves dimension has a 128-byte stride inside each
+// row, so the box lands in shared memory as kh blocks of [half][rows][128 B].
+bool encode_page_5d(CUtensorMap* map, const void* base, int D, int page_size, int Hkv,
+                    int64_t num_pages, cuuint32_t box_rows, int kh) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t row_bytes = 256;   // D = 128
-    const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(page_size), 2,
-                                static_cast<cuuint64_t>(num_pages) * Hkv};
-    const cuuint64_t strides[3] = {row_bytes, 128, row_bytes * page_size};
-    const cuuint32_t box[4] = {64, box_rows, 2, 1};
-    const cuuint32_t estride[4] = {1, 1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(D) * 2;
+    const cuuint64_t halves = static_cast<cuuint64_t>(D / 64);
+    const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(page_size), halves,
+                                static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(num_pages)};
+    const cuuint64_t strides[4] = {row_bytes, 128, row_bytes * page_size,
+                                   row_bytes * page_size * Hkv};
+    const cuuint32_t box[5] = {64, box_rows, static_cast<cuuint32_t>(halves),
+                               static_cast<cuuint32_t>(kh), 1};
+    const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
               estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -267,6 +283,16 @@ size_t decode_attn_workspace_size(int variant, int B, int Hq, int Hkv, int D, in
         if (dev < 0) return 0;
         const int sms = sm_count(dev);
         if (sms <= 0) return 0;
+        if (variant == DA_VARIANT_PAGED) {
+            // the page size is not an argument here: size for every unit width a call may use
+            size_t most = 0;
+            for (int kh = 1; kh <= 8; kh *= 2) {
+                if (Hkv % kh != 0 || kh * G > 64) break;
+                const long long u = units / kh;
+                most = std::max(most, ws_layout(u, u + sms, kh * G, D).total);
+            }
+            return most;
+        }
         segments = units + sms;
     } else if (variant == DA_VARIANT_SPARSE) {
         if (max_kv < 0) return 0;
@@ -369,27 +395,33 @@ da_status decode_attn_paged(const void* q, const void* k_pool, const void* v_poo
     if (dev < 0) return DA_ERR_CUDA;
     const int sms = sm_count(dev);
     if (sms <= 0) return DA_ERR_CUDA;
-    const int G = Hq / Hkv, GP = padded_group(G);
-    const WsLayout w = ws_layout(units, units + sms, G, D);
-    if (workspace_bytes < w.total) return DA_ERR_WORKSPACE_TOO_SMALL;
-
+    const int G = Hq / Hkv;
     Launch L{};
     const cuuint64_t row_bytes = static_cast<cuuint64_t>(D) * 2;
     const cuuint64_t page_bytes = row_bytes * page_size * Hkv;
-    const cuuint32_t box_rows = static_cast<cuuint32_t>(std::min(page_size, kTileKeys));
-    // D = 128: one box per page and tensor when the driver accepts the 4-D descriptor; else (and
-    // for D = 64, whose page is a single 128-byte-wide box anyway) one 3-D box per half.
-    int box_4d = 0;
-    if (D == 128 && static_cast<long long>(num_pages) * Hkv < (1ll << 31) &&
-        encode_page_4d(&L.tm_k, k_pool, page_size, Hkv, num_pages, box_rows) &&
-        encode_page_4d(&L.tm_v, v_pool, page_size, Hkv, num_pages, box_rows))
-        box_4d = 1;
-    if (!box_4d &&
-        (!encode_3d(&L.tm_k, k_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
-                    row_bytes, page_bytes, box_rows) ||
-         !encode_3d(&L.tm_v, v_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
-                    row_bytes, page_bytes, box_rows)))
-        return DA_ERR_CUDA;
+    // One 5-D box per page and tensor carrying kh KV heads and both halves; if the driver
+    // refuses that descriptor, one KV head per unit and one 3-D box per half.
+    int kh = paged_kv_heads(Hkv, G, page_size, D);
+    int box_nd = 0;
+    {
+        const cuuint32_t rows = static_cast<cuuint32_t>(std::min(page_size, kTileKeys / kh));
+        if (encode_page_5d(&L.tm_k, k_pool, D, page_size, Hkv, num_pages, rows, kh) &&
+            encode_page_5d(&L.tm_v, v_pool, D, page_size, Hkv, num_pages, rows, kh))
+            box_nd = 1;
+    }
+    if (!box_nd) {
+        kh = 1;
+        const cuuint32_t rows = static_cast<cuuint32_t>(std::min(page_size, kTileKeys));
+        if (!encode_3d(&L.tm_k, k_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
+                       row_bytes, page_bytes, rows) ||
+            !encode_3d(&L.tm_v, v_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
+                       row_bytes, page_bytes, rows))
+            return DA_ERR_CUDA;
+    }
+    const int GP = padded_group(kh * G);
+    const long long punits = units / kh;
+    const WsLayout w = ws_layout(punits, punits + sms, kh * G, D);
+    if (workspace_bytes < w.total) return DA_ERR_WORKSPACE_TOO_SMALL;
     L.p = base_params(q, out, B, Hq, Hkv, softmax_scale, device_error_ptr(dev));
     bind_workspace(L.p, workspace, w);
     L.p.block_table = block_table;
@@ -398,7 +430,10 @@ da_status decode_attn_paged(const void* q, const void* k_pool, const void* v_poo
     L.p.num_pages = static_cast<int>(num_pages);
     L.p.kv_lens = kv_lens;
     L.p.kv_stride = kv_len_stride;
-    L.p.page_box_4d = box_4d;
+    L.p.page_box_nd = box_nd;
+    L.p.kh = kh;
+    L.p.tile_keys = kTileKeys / kh;
+    L.p.seg_heads = kh * G;
     L.grid = persistent_ctas(dev);
     L.stream = cs;
     return launch_paged(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;

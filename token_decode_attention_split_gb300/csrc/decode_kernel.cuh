@@ -1,7 +1,9 @@
 // Single-query decode attention on sm_103a: one kernel per call.
 //
 // Work decomposition.  A "unit" is one (sequence b, KV head g); its G = Hq/Hkv query heads are
-// processed together so every K/V row is read from HBM exactly once.  A unit's live rows are cut
+// processed together so every K/V row is read from HBM exactly once.  Paged units may take kh
+// adjacent KV heads (kh * G query heads) so that one TMA box carries a whole page of all kh
+// heads; each query-head column then only sees the rows of its own KV head.  A unit's live rows are cut
 // into 64-row tiles.  Dense and paged calls run a persistent grid (one CTA per SM): the tiles of
 // all units are laid end to end and CTA c takes the contiguous range [c*N/C, (c+1)*N/C), so the
 // load is balanced to one tile whatever the lengths.  Sparse calls give each CTA up to 16 query
@@ -92,7 +94,9 @@ struct Params {
     // paged
     const int* block_table;
     int max_pages, page_size, num_pages;
-    int page_box_4d;          // 1: one 4-D box per page (both halves), 0: one 3-D box per half
+    int page_box_nd;          // 1: one 5-D box per page (kh heads, both halves); 0: 3-D per half
+    int kh;                   // KV heads per unit (paged; 1 otherwise), a power of two
+    int tile_keys;            // keys per stage and KV head: 64 / kh
     const unsigned* kv_lens;
     int kv_stride;
     // sparse
@@ -198,23 +202,25 @@ __device__ __forceinline__ Unit locate_dense(const Params& p, int t) {
     return U;
 }
 
+// Paged units: (b, KV-head group gk of kh heads), gk fastest; U.g is gk.
 __device__ __forceinline__ Unit locate_paged(const Params& p, const SmemPtrs& sm, int t) {
-    // largest b with seq_prefix[b] * Hkv <= t
+    const int upb = p.Hkv / p.kh;   // units per sequence
+    // largest b with seq_prefix[b] * upb <= t
     int lo = 0, hi = p.B - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (sm.seq_prefix[mid] * p.Hkv <= t) lo = mid; else hi = mid - 1;
+        if (sm.seq_prefix[mid] * upb <= t) lo = mid; else hi = mid - 1;
     }
     Unit U;
     U.b = lo;
     U.nt = sm.seq_prefix[lo + 1] - sm.seq_prefix[lo];
-    const int r = t - sm.seq_prefix[lo] * p.Hkv;
+    const int r = t - sm.seq_prefix[lo] * upb;
     U.g = r / U.nt;
-    U.u = U.b * p.Hkv + U.g;
+    U.u = U.b * upb + U.g;
     U.len = sm.seq_len[lo];
-    U.base = sm.seq_prefix[lo] * p.Hkv + U.g * U.nt;
-    U.hq0 = U.b * p.Hq + U.g * p.G;
-    U.nh = p.G;
+    U.base = sm.seq_prefix[lo] * upb + U.g * U.nt;
+    U.hq0 = U.b * p.Hq + U.g * p.kh * p.G;
+    U.nh = p.kh * p.G;
     U.cu = U.u;
     return U;
 }
@@ -228,13 +234,18 @@ struct ConsumerState {
     float o[Gm::DT][Gm::NT][4];           // O^T accumulator fragments
     float m_run[Gm::NT][2];               // running max (log2 domain) of heads 2qd, 2qd+1
     float l_run[Gm::NT][2];               // this thread's share of the running sum
+    int col_kv[Gm::NT][2];                // KV head (within the unit) of each of those columns
 
-    __device__ __forceinline__ void init(int warp, int lane_) {
+    __device__ __forceinline__ void init(int warp, int lane_, int G) {
         lane = lane_;
         hg = warp % Gm::HS;
         kg = warp / Gm::HS;
         gq = lane >> 2;
         qd = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) col_kv[nt][hc] = head_of(nt, hc) / G;
     }
 
     __device__ __forceinline__ int head_of(int nt, int hc) const {
@@ -272,8 +283,10 @@ struct ConsumerState {
     }
 
     // One stage: this warp's MT*16 rows of the tile.  `mask` bit r = row r of the tile is valid.
+    // kh > 1: tile rows come in blocks of 2^rb_shift rows cycling over the unit's kh KV heads, and
+    // a score is kept only where the row's KV head is the column's.
     __device__ __forceinline__ void consume(uint32_t k_tile, uint32_t v_tile, uint64_t mask,
-                                            float scale_log2, int rb_shift) {
+                                            float scale_log2, int rb_shift, int kh) {
         constexpr int kRows = Gm::MT * 16;
         const uint64_t rows_mask = kRows == 64 ? ~0ull : ((1ull << kRows) - 1ull);
         const uint64_t wmask = (mask >> (kg * kRows)) & rows_mask;
@@ -301,7 +314,7 @@ struct ConsumerState {
             }
         }
 
-        // scale into the log2 domain; invalid rows -> -inf
+        // scale into the log2 domain; invalid rows (and other KV heads' rows) -> -inf
 #pragma unroll
         for (int mt = 0; mt < Gm::MT; ++mt)
 #pragma unroll
@@ -309,10 +322,10 @@ struct ConsumerState {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float x = s[mt][nt][e] * scale_log2;
-                    if (!all_valid) {
-                        const int rr = mt * 16 + gq + (e >= 2 ? 8 : 0);
-                        if (!((wmask >> rr) & 1ull)) x = -CUDART_INF_F;
-                    }
+                    const int rr = mt * 16 + gq + (e >= 2 ? 8 : 0);
+                    if (!all_valid && !((wmask >> rr) & 1ull)) x = -CUDART_INF_F;
+                    if (kh > 1 && (((row0 + rr) >> rb_shift) & (kh - 1)) != col_kv[nt][e & 1])
+                        x = -CUDART_INF_F;
                     s[mt][nt][e] = x;
                 }
 
@@ -478,6 +491,23 @@ __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, 
 #pragma unroll
     for (int j = 0; j < NH; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
 
+    // Few segments (the usual case): issue the partial-row loads now, together with the LSE
+    // loads below, so the merge costs one L2 round trip instead of two.
+    // (Not for 64-head groups, whose 16 rows per thread would not fit the register budget.)
+    constexpr bool kPrefetch = NH <= 8;
+    constexpr int PU = kPrefetch ? SU : 1, PH = kPrefetch ? NH : 1;
+    const bool prefetched = kPrefetch && one_batch && nseg <= SU;
+    float4 pre[PU][PH];
+#pragma unroll
+    for (int u = 0; u < PU; ++u)
+#pragma unroll
+        for (int j = 0; j < PH; ++j) {
+            const int h = hq + j * HQ;
+            pre[u][j] = (prefetched && u < nseg && h < G)
+                            ? __ldcg(orow + (static_cast<size_t>(u) * SH + h) * D4 + d4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+
     for (int s0 = 0; s0 < nseg; s0 += SB) {
         const int nb = min(SB, nseg - s0);
         for (int i = tid; i < nb * G; i += kConsumerThreads) {
@@ -524,9 +554,12 @@ __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, 
                 for (int j = 0; j < NH; ++j) {
                     const int h = hq + j * HQ;
                     w[u][j] = (sgi + u < nb && h < G) ? w_sm[(sgi + u) * GP + h] : 0.f;
-                    o4[u][j] = w[u][j] != 0.f
-                                   ? __ldcg(orow + (static_cast<size_t>(s0 + sgi + u) * SH + h) * D4 + d4)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (prefetched)
+                        o4[u][j] = pre[kPrefetch ? u : 0][kPrefetch ? j : 0];
+                    else
+                        o4[u][j] = w[u][j] != 0.f
+                                       ? __ldcg(orow + (static_cast<size_t>(s0 + sgi + u) * SH + h) * D4 + d4)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
             for (int u = 0; u < SU; ++u)
@@ -668,7 +701,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             const unsigned raw = __ldg(p.kv_lens + static_cast<size_t>(b) * p.kv_stride);
             const int len = raw > static_cast<unsigned>(cap) ? cap : static_cast<int>(raw);
             sm.seq_len[b] = len;
-            sm.seq_prefix[b + 1] = (len + kTileKeys - 1) / kTileKeys;
+            sm.seq_prefix[b + 1] = (len + p.tile_keys - 1) / p.tile_keys;
         }
         __syncthreads();
         if (warp == 0) {
@@ -693,7 +726,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         N = p.B * p.Hkv * p.dense_tiles;
         C = gridDim.x;
     } else if (VAR == kPaged) {
-        N = sm.seq_prefix[p.B] * p.Hkv;
+        N = sm.seq_prefix[p.B] * (p.Hkv / p.kh);
         C = min(static_cast<int>(gridDim.x), N);
     }
     if (VAR != kSparse && static_cast<int>(blockIdx.x) < C && N > 0) {
@@ -748,13 +781,16 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 const uint64_t mask = static_cast<uint64_t>(__ballot_sync(0xffffffffu, v0)) |
                                       (static_cast<uint64_t>(__ballot_sync(0xffffffffu, v1)) << 32);
                 unsigned char* tile = sm.stages + s * Gm::kStageBytes + (isv ? Gm::kTileBytes : 0);
-#pragma unroll 4
+                const __nv_bfloat16* base = pool + static_cast<size_t>(sp_u) * p.pool_rows * D + c * 8;
+                // independent iterations: each lane reads its row's entry from shared memory, so
+                // the unrolled loop keeps several index reads and copies in flight
+#pragma unroll 8
                 for (int rb = 0; rb < kTileKeys; rb += kRowsPerInstr) {
                     const int r = rb + sub;
-                    const int idx = __shfl_sync(0xffffffffu, rb < 32 ? idx0 : idx1, r & 31);
-                    const bool valid = (mask >> r) & 1ull;
-                    const __nv_bfloat16* src =
-                        pool + (static_cast<size_t>(sp_u) * p.pool_rows + (valid ? idx : 0)) * D + c * 8;
+                    const int li = l0 + r;
+                    const int idx = li < sp_nkeys ? sidx[li] : -1;
+                    const bool valid = idx >= 0;
+                    const __nv_bfloat16* src = base + static_cast<size_t>(valid ? idx : 0) * D;
                     cp_async_16(tile + tile_offset<Gm::kHalves>(r, c, 6), src, valid ? 16u : 0u);
                 }
                 if (lane == 0) sm.stage_mask[s] = mask;
@@ -769,9 +805,11 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         } else {
             // dense / paged: lane 0 issues TMA; paged uses all lanes to fetch block-table entries
             const int P = p.page_size;
-            const int box_rows = VAR == kPaged ? min(P, kTileKeys) : kTileKeys;
-            const int pages_per_tile = VAR == kPaged ? (P >= kTileKeys ? 1 : kTileKeys / P) : 1;
+            const int TK = VAR == kPaged ? p.tile_keys : kTileKeys;   // keys per stage and KV head
+            const int box_rows = VAR == kPaged ? min(P, TK) : kTileKeys;
+            const int pages_per_tile = VAR == kPaged ? (P >= TK ? 1 : TK / P) : 1;
             const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * 128u;
+            const uint64_t box_mask = box_rows >= 64 ? ~0ull : ((1ull << box_rows) - 1ull);
             int bt_b = -1, bt_base = -1;   // current batch: slots [bt_base, bt_base + 32) of sequence bt_b
             int bt_cur = -1, bt_nxt = -1;
             for (int t = t0; t < t1 && ok;) {
@@ -783,8 +821,8 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     const uint32_t ph = (it / S) & 1;
                     if (!mbar_wait(sm.empty + s, ph ^ 1u, sm.abort, kWaitLimitNs)) { ok = false; break; }
                     const int j = t - U.base;
-                    const int key0 = j * kTileKeys;
-                    const int nvalid = min(kTileKeys, U.len - key0);
+                    const int key0 = j * TK;
+                    const int nvalid = min(TK, U.len - key0);
                     uint64_t mask = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
                     unsigned char* ktile = sm.stages + s * Gm::kStageBytes;
                     unsigned char* vtile = ktile + Gm::kTileBytes;
@@ -814,7 +852,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                             const int sn = want + 32 + lane;
                             bt_nxt = sn < npages_seq ? __ldg(row + sn) : -1;
                         }
-                        const int row_in_page = P > kTileKeys ? key0 % P : 0;
+                        const int row_in_page = P > TK ? key0 % P : 0;
                         uint32_t page_ok = 0;
                         int pages[8];
 #pragma unroll
@@ -825,22 +863,30 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                                 page_ok |= 1u << i;
                         }
                         if (lane == 0) {
+                            // rows of the tile: page i, then KV head hh of the unit, then slot
                             uint32_t nloaded = 0;
-                            for (int i = 0; i < pages_per_tile; ++i) {
-                                if (page_ok & (1u << i)) { ++nloaded; continue; }
-                                const uint64_t pm = (box_rows >= 64 ? ~0ull : ((1ull << box_rows) - 1ull)) << (i * box_rows);
-                                mask &= ~pm;
-                            }
-                            sm.stage_mask[s] = mask;
-                            mbar_arrive_expect_tx(sm.full + s, nloaded * 2u * Gm::kHalves * box_bytes);
+                            uint64_t rows = 0;
                             for (int i = 0; i < pages_per_tile; ++i) {
                                 if (!(page_ok & (1u << i))) continue;
-                                // block i of the tile: its halves one after the other
-                                const int dst = i * Gm::kHalves * box_rows * 128;
-                                if (p.page_box_4d) {
-                                    const int ph = pages[i] * p.Hkv + U.g;
-                                    tma_load_4d(ktile + dst, &tm_k, 0, row_in_page, 0, ph, sm.full + s);
-                                    tma_load_4d(vtile + dst, &tm_v, 0, row_in_page, 0, ph, sm.full + s);
+                                ++nloaded;
+                                const int nv = min(box_rows, U.len - (key0 + i * box_rows));
+                                if (nv <= 0) continue;
+                                const uint64_t bits = nv >= 64 ? ~0ull : ((1ull << nv) - 1ull);
+                                for (int hh = 0; hh < p.kh; ++hh)
+                                    rows |= (bits & box_mask) << ((i * p.kh + hh) * box_rows);
+                            }
+                            mask = rows;
+                            sm.stage_mask[s] = mask;
+                            mbar_arrive_expect_tx(sm.full + s,
+                                                  nloaded * 2u * p.kh * Gm::kHalves * box_bytes);
+                            for (int i = 0; i < pages_per_tile; ++i) {
+                                if (!(page_ok & (1u << i))) continue;
+                                // blocks i*kh .. i*kh+kh-1 of the tile, halves one after the other
+                                const int dst = i * p.kh * Gm::kHalves * box_rows * 128;
+                                if (p.page_box_nd) {
+                                    const int h0 = U.g * p.kh;
+                                    tma_load_5d(ktile + dst, &tm_k, 0, row_in_page, 0, h0, pages[i], sm.full + s);
+                                    tma_load_5d(vtile + dst, &tm_v, 0, row_in_page, 0, h0, pages[i], sm.full + s);
                                 } else {
 #pragma unroll
                                     for (int h = 0; h < Gm::kHalves; ++h) {
@@ -873,19 +919,18 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
 
     // ==================================================================== consumer warps
-    const int rb_shift = VAR == kPaged ? 31 - __clz(min(p.page_size, kTileKeys)) : 6;
+    const int rb_shift = VAR == kPaged ? 31 - __clz(min(p.page_size, p.tile_keys)) : 6;
+    const int kh = VAR == kPaged ? p.kh : 1;
     ConsumerState<D, GP> cs;
-    cs.init(warp, lane);
+    cs.init(warp, lane, p.G);
     uint32_t gphase = 0;
 
     if (VAR == kPaged) {
-        // units with no rows get a zero row (null-row convention)
-        const int units = p.B * p.Hkv;
-        for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const int b = u / p.Hkv, g = u - b * p.Hkv;
+        // sequences with no rows get zero rows (null-row convention)
+        for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
             if (sm.seq_len[b] != 0) continue;
-            for (int idx = threadIdx.x; idx < p.G * D; idx += kConsumerThreads)
-                p.out[(static_cast<size_t>(b) * p.Hq + static_cast<size_t>(g) * p.G) * D + idx] = __float2bfloat16_rn(0.f);
+            for (int idx = threadIdx.x; idx < p.Hq * D; idx += kConsumerThreads)
+                p.out[static_cast<size_t>(b) * p.Hq * D + idx] = __float2bfloat16_rn(0.f);
         }
     }
 
@@ -913,7 +958,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 return;
             }
             const uint32_t ktile = smem_u32(sm.stages + s * Gm::kStageBytes);
-            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2, rb_shift);
+            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2, rb_shift, kh);
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty + s);
         }
@@ -942,7 +987,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 return;
             }
             const uint32_t ktile = smem_u32(sm.stages + s * Gm::kStageBytes);
-            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2, rb_shift);
+            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2, rb_shift, kh);
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty + s);
         }
