@@ -17,6 +17,9 @@ What each function computes, with the page each follows:
     selection whose -1 entries add nothing.
   * ``dense_range`` -- the same dense definition restricted to rows [j0, j1), returning the
     normalised row and its natural-log log-sum-exp (for the split/merge identity tests).
+  * ``append_paged`` -- "DflashScratch", field slot_mapping_dev (reshape_and_cache): new K/V rows
+    scattered to paged-cache slots; ``append_ring`` -- "AttnV41", method decode_body: the ring
+    write at pos % window.  Both return updated copies of the pools.
 """
 from __future__ import annotations
 
@@ -68,7 +71,10 @@ def _load():
                                       i64p, i64, i]
         lib.oracle_dense_range.argtypes = [u16p, u16p, u16p, i, i, i, i, i64, i, i, i64, i64, d,
                                            f64p, f64p]
-        for f in (lib.oracle_dense, lib.oracle_paged, lib.oracle_sparse, lib.oracle_dense_range):
+        lib.oracle_append_paged.argtypes = [u16p, u16p, u16p, u16p, i64p, i64, i, i, i64, i64]
+        lib.oracle_append_ring.argtypes = [u16p, u16p, u16p, u16p, i64p, i, i, i, i64, i64]
+        for f in (lib.oracle_dense, lib.oracle_paged, lib.oracle_sparse, lib.oracle_dense_range,
+                  lib.oracle_append_paged, lib.oracle_append_ring):
             f.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -180,3 +186,36 @@ def dense_range(q, k, v, b: int, h: int, j0: int, j1: int, scale: float):
                                     float(scale), _ptr(o, ctypes.c_double), ctypes.byref(lse))
     _check(rc, "dense_range")
     return o, lse.value
+
+
+def append_paged(k_new, v_new, k_pool, v_pool, slot_mapping):
+    """k_new, v_new [T,Hkv,D]; pools [num_pages,Hkv,page_size,D]; slot_mapping int64 [T].
+    Returns (k_pool', v_pool') as new uint16 arrays; the inputs are not modified."""
+    kn, vn = _bits(k_new), _bits(v_new)
+    kp, vp = _bits(k_pool).copy(), _bits(v_pool).copy()
+    sm = np.ascontiguousarray(np.asarray(slot_mapping, dtype=np.int64).reshape(-1))
+    T = sm.size
+    num_pages, Hkv, P, D = kp.shape
+    if kn.size != T * Hkv * D or vn.size != kn.size:
+        raise ValueError("k_new / v_new must be [T, Hkv, D]")
+    rc = _load().oracle_append_paged(_ptr(kn, ctypes.c_uint16), _ptr(vn, ctypes.c_uint16),
+                                     _ptr(kp, ctypes.c_uint16), _ptr(vp, ctypes.c_uint16),
+                                     _ptr(sm, ctypes.c_int64), T, Hkv, D, P, num_pages)
+    _check(rc, "append_paged")
+    return kp, vp
+
+
+def append_ring(k_new, v_new, k_pool, v_pool, positions, window: int):
+    """k_new, v_new [B,Hkv,D]; pools [B,Hkv,pool_rows,D]; positions int64 [B].
+    Returns (k_pool', v_pool') as new uint16 arrays; the inputs are not modified."""
+    kn, vn = _bits(k_new), _bits(v_new)
+    kp, vp = _bits(k_pool).copy(), _bits(v_pool).copy()
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64).reshape(-1))
+    B, Hkv, R, D = kp.shape
+    if pos.size != B or kn.size != B * Hkv * D or vn.size != kn.size:
+        raise ValueError("k_new / v_new must be [B, Hkv, D] and positions [B]")
+    rc = _load().oracle_append_ring(_ptr(kn, ctypes.c_uint16), _ptr(vn, ctypes.c_uint16),
+                                    _ptr(kp, ctypes.c_uint16), _ptr(vp, ctypes.c_uint16),
+                                    _ptr(pos, ctypes.c_int64), B, Hkv, D, R, int(window))
+    _check(rc, "append_ring")
+    return kp, vp

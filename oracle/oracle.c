@@ -293,3 +293,60 @@ int oracle_dense_range(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     free(s);
     return ORACLE_OK;
 }
+
+/*
+ * KV append (the step before the hot path), restated from:
+ *   - "DflashScratch" (docs.metrale.ai, dflash_head), field slot_mapping_dev: i64 paged-cache
+ *     slot per new row, used by reshape_and_cache.  Row t of k_new / v_new ([T, Hkv, D]) goes to
+ *     slot s = slot_mapping[t]: page s / page_size, position s % page_size, for every KV head.
+ *     Reading: a slot outside [0, num_pages * page_size) (the usual -1 padding entry, or any
+ *     other) writes nothing.
+ *   - "AttnV41" (docs.metrale.ai, attn_v41), method decode_body: the window ring write at
+ *     pos % window with the slot read on the device.  Row b of k_new / v_new ([B, Hkv, D]) goes to
+ *     ring row positions[b] % window of sequence b's pool [B, Hkv, pool_rows, D].  Reading: a
+ *     negative position writes nothing.
+ * Plain element copies; later rows win when two rows name the same slot (rows in order).
+ */
+int oracle_append_paged(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_pool,
+                        uint16_t *v_pool, const int64_t *slot_mapping, int64_t T, int Hkv, int D,
+                        int64_t page_size, int64_t num_pages) {
+    if (!k_new || !v_new || !k_pool || !v_pool || !slot_mapping || T < 0 || Hkv <= 0 || D <= 0 ||
+        page_size <= 0 || num_pages < 0)
+        return ORACLE_EINVAL;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0 || slot >= num_pages * page_size) continue;
+        const int64_t page = slot / page_size, off = slot % page_size;
+        for (int g = 0; g < Hkv; ++g) {
+            const int64_t src = (t * Hkv + g) * (int64_t)D;
+            const int64_t dst = ((page * Hkv + g) * page_size + off) * (int64_t)D;
+            for (int d = 0; d < D; ++d) {
+                k_pool[dst + d] = k_new[src + d];
+                v_pool[dst + d] = v_new[src + d];
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+int oracle_append_ring(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_pool,
+                       uint16_t *v_pool, const int64_t *positions, int B, int Hkv, int D,
+                       int64_t pool_rows, int64_t window) {
+    if (!k_new || !v_new || !k_pool || !v_pool || !positions || B < 0 || Hkv <= 0 || D <= 0 ||
+        window <= 0 || window > pool_rows)
+        return ORACLE_EINVAL;
+    for (int b = 0; b < B; ++b) {
+        const int64_t pos = positions[b];
+        if (pos < 0) continue;
+        const int64_t row = pos % window;
+        for (int g = 0; g < Hkv; ++g) {
+            const int64_t src = ((int64_t)b * Hkv + g) * D;
+            const int64_t dst = (((int64_t)b * Hkv + g) * pool_rows + row) * D;
+            for (int d = 0; d < D; ++d) {
+                k_pool[dst + d] = k_new[src + d];
+                v_pool[dst + d] = v_new[src + d];
+            }
+        }
+    }
+    return ORACLE_OK;
+}
