@@ -155,36 +155,14 @@ bool encode_3d(CUtensorMap* map, const void* base, cuuint64_t d0, cuuint64_t d1,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// KV heads per paged unit: the smallest power of two that makes one page of those heads at least
-// 8 KB (a TMA box that size streams at full rate; a 4 KB one does not), limited so the unit's
-// query heads fit one CTA (kh * G <= 64), kh divides Hkv, and a stage keeps >= 8 keys per head.
-int paged_kv_heads(int Hkv, int G, int page_size, int D) {
+// KV heads per paged unit: the smallest power of two that makes a page of those heads (kh adjacent
+// heads are kh * page_size contiguous rows) at least one 64-row tile, so a paged tile moves as one
+// 64-row TMA box per 64-column half, exactly like a dense tile; limited so kh divides Hkv and the
+// unit's kh * G query heads fit one CTA.
+int paged_kv_heads(int Hkv, int G, int page_size) {
     int kh = 1;
-    while (kh < 8 && static_cast<long long>(kh) * page_size * D * 2 < 8192 && Hkv % (2 * kh) == 0 &&
-           2 * kh * G <= 64)
-        kh *= 2;
+    while (kh * page_size < kTileKeys && Hkv % (2 * kh) == 0 && 2 * kh * G <= 64) kh *= 2;
     return kh;
-}
-
-// One page of kh adjacent KV heads as a single box: dims (64 columns, rows of a page, the
-// 64-column halves, KV heads, pages).  The halves dimension has a 128-byte stride inside each
-// row, so the box lands in shared memory as kh blocks of [half][rows][128 B].
-bool encode_page_5d(CUtensorMap* map, const void* base, int D, int page_size, int Hkv,
-                    int64_t num_pages, cuuint32_t box_rows, int kh) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t row_bytes = static_cast<cuuint64_t>(D) * 2;
-    const cuuint64_t halves = static_cast<cuuint64_t>(D / 64);
-    const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(page_size), halves,
-                                static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(num_pages)};
-    const cuuint64_t strides[4] = {row_bytes, 128, row_bytes * page_size,
-                                   row_bytes * page_size * Hkv};
-    const cuuint32_t box[5] = {64, box_rows, static_cast<cuuint32_t>(halves),
-                               static_cast<cuuint32_t>(kh), 1};
-    const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
-              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // CTAs for a persistent dense/paged launch on `dev`.
@@ -245,7 +223,7 @@ cudaError_t launch_kernel(const void* kernel, int smem, const Launch& L) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(L.threads);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = L.stream;
     cfg.attrs = attr;
@@ -366,6 +344,7 @@ da_status decode_attn_dense(const void* q, const void* k, const void* v, void* o
     const long long N = units * tiles;
     L.grid = static_cast<int>(std::min<long long>(persistent_ctas(dev), N));
     L.stream = cs;
+    L.threads = Roles<kDense>::kThreads;
     return launch_dense(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
@@ -399,25 +378,15 @@ da_status decode_attn_paged(const void* q, const void* k_pool, const void* v_poo
     Launch L{};
     const cuuint64_t row_bytes = static_cast<cuuint64_t>(D) * 2;
     const cuuint64_t page_bytes = row_bytes * page_size * Hkv;
-    // One 5-D box per page and tensor carrying kh KV heads and both halves; if the driver
-    // refuses that descriptor, one KV head per unit and one 3-D box per half.
-    int kh = paged_kv_heads(Hkv, G, page_size, D);
-    int box_nd = 0;
-    {
-        const cuuint32_t rows = static_cast<cuuint32_t>(std::min(page_size, kTileKeys / kh));
-        if (encode_page_5d(&L.tm_k, k_pool, D, page_size, Hkv, num_pages, rows, kh) &&
-            encode_page_5d(&L.tm_v, v_pool, D, page_size, Hkv, num_pages, rows, kh))
-            box_nd = 1;
-    }
-    if (!box_nd) {
-        kh = 1;
-        const cuuint32_t rows = static_cast<cuuint32_t>(std::min(page_size, kTileKeys));
-        if (!encode_3d(&L.tm_k, k_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
-                       row_bytes, page_bytes, rows) ||
-            !encode_3d(&L.tm_v, v_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
-                       row_bytes, page_bytes, rows))
-            return DA_ERR_CUDA;
-    }
+    // Pools viewed as [num_pages][Hkv * page_size rows][D]; a box is min(kh * page_size, 64)
+    // rows of one page (kh adjacent heads) by one 64-column half.
+    const int kh = paged_kv_heads(Hkv, G, page_size);
+    const cuuint32_t rows = static_cast<cuuint32_t>(std::min(kh * page_size, kTileKeys));
+    if (!encode_3d(&L.tm_k, k_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
+                   row_bytes, page_bytes, rows) ||
+        !encode_3d(&L.tm_v, v_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
+                   row_bytes, page_bytes, rows))
+        return DA_ERR_CUDA;
     const int GP = padded_group(kh * G);
     const long long punits = units / kh;
     const WsLayout w = ws_layout(punits, punits + sms, kh * G, D);
@@ -430,12 +399,12 @@ da_status decode_attn_paged(const void* q, const void* k_pool, const void* v_poo
     L.p.num_pages = static_cast<int>(num_pages);
     L.p.kv_lens = kv_lens;
     L.p.kv_stride = kv_len_stride;
-    L.p.page_box_nd = box_nd;
     L.p.kh = kh;
     L.p.tile_keys = kTileKeys / kh;
     L.p.seg_heads = kh * G;
     L.grid = persistent_ctas(dev);
     L.stream = cs;
+    L.threads = Roles<kPaged>::kThreads;
     return launch_paged(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
@@ -477,6 +446,7 @@ da_status decode_attn_sparse(const void* q, const void* k_pool, const void* v_po
     L.p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
     L.grid = static_cast<int>(groups * chunks);
     L.stream = cs;
+    L.threads = Roles<kSparse>::kThreads;
     return launch_sparse(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 

@@ -2,8 +2,9 @@
 //
 // Work decomposition.  A "unit" is one (sequence b, KV head g); its G = Hq/Hkv query heads are
 // processed together so every K/V row is read from HBM exactly once.  Paged units may take kh
-// adjacent KV heads (kh * G query heads) so that one TMA box carries a whole page of all kh
-// heads; each query-head column then only sees the rows of its own KV head.  A unit's live rows are cut
+// adjacent KV heads (kh * G query heads): a page of kh adjacent heads is kh * page_size
+// contiguous rows, so with kh * page_size = 64 a paged tile is one 64-row TMA box per half, the
+// same transfer as a dense tile; each query-head column then only sees its own KV head's rows.  A unit's live rows are cut
 // into 64-row tiles.  Dense and paged calls run a persistent grid (one CTA per SM): the tiles of
 // all units are laid end to end and CTA c takes the contiguous range [c*N/C, (c+1)*N/C), so the
 // load is balanced to one tile whatever the lengths.  Sparse calls give each CTA up to 16 query
@@ -44,7 +45,13 @@ namespace da {
 constexpr int kTileKeys = 64;                 // K/V rows per pipeline stage
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+// Producer warps per CTA: one TMA-issuing warp for dense and paged; the sparse gather issues
+// 16-byte cp.async copies, and one warp cannot keep enough of them in flight, so it gets four.
+template <int VAR>
+struct Roles {
+    static constexpr int kProducerWarps = VAR == 2 ? 4 : 1;
+    static constexpr int kThreads = kConsumerThreads + 32 * kProducerWarps;
+};
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr int kSparseHeadGroup = 16;         // query heads per CTA when a group is split
 constexpr int kSparseChunkUnit = 512;         // sparse chunk = 512 entries per head group
@@ -94,7 +101,6 @@ struct Params {
     // paged
     const int* block_table;
     int max_pages, page_size, num_pages;
-    int page_box_nd;          // 1: one 5-D box per page (kh heads, both halves); 0: 3-D per half
     int kh;                   // KV heads per unit (paged; 1 otherwise), a power of two
     int tile_keys;            // keys per stage and KV head: 64 / kh
     const unsigned* kv_lens;
@@ -234,18 +240,57 @@ struct ConsumerState {
     float o[Gm::DT][Gm::NT][4];           // O^T accumulator fragments
     float m_run[Gm::NT][2];               // running max (log2 domain) of heads 2qd, 2qd+1
     float l_run[Gm::NT][2];               // this thread's share of the running sum
-    int col_kv[Gm::NT][2];                // KV head (within the unit) of each of those columns
+    // Per-kernel constants of this lane, set once by init():
+    uint32_t k_row_off[Gm::MT];           // byte offset of this lane's K ldmatrix row, chunk 0
+    uint32_t v_row_off[Gm::MT];           // same for the transposed V ldmatrix
+    uint32_t half_stride;                 // bytes between the two 64-column halves of a block
+    uint32_t col_ok;                      // bit (mt*NT + nt)*4 + e: score element may be kept
+    uint32_t need;                        // bit mt*NT + nt: the n-tile can see the m-tile's rows
+    uint32_t nt_any;                      // bit nt: some m-tile of this warp needs n-tile nt
 
-    __device__ __forceinline__ void init(int warp, int lane_, int G) {
+    // rb_shift: log2 of the rows per block of the tile layout; kh > 1 (paged units of kh KV
+    // heads): row r of the tile belongs to the unit's KV head (r >> head_shift) & (kh - 1), and a
+    // query-head column c to KV head c / G.
+    __device__ __forceinline__ void init(int warp, int lane_, int G, int kh, int rb_shift,
+                                         int head_shift) {
         lane = lane_;
         hg = warp % Gm::HS;
         kg = warp / Gm::HS;
         gq = lane >> 2;
         qd = lane & 3;
+        const int row0 = kg * Gm::MT * 16;
+        half_stride = 1u << (rb_shift + 7);
+        auto block_row = [&](int r) -> uint32_t {
+            return static_cast<uint32_t>((((r >> rb_shift) * Gm::kHalves) << (rb_shift + 7)) +
+                                         (r & ((1 << rb_shift) - 1)) * 128);
+        };
+        col_ok = 0;
+        need = 0;
+        nt_any = 0;
 #pragma unroll
-        for (int nt = 0; nt < Gm::NT; ++nt)
+        for (int mt = 0; mt < Gm::MT; ++mt) {
+            k_row_off[mt] = block_row(row0 + mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8);
+            v_row_off[mt] = block_row(row0 + mt * 16 + (lane & 7) + ((lane >> 4) << 3));
 #pragma unroll
-            for (int hc = 0; hc < 2; ++hc) col_kv[nt][hc] = head_of(nt, hc) / G;
+            for (int nt = 0; nt < Gm::NT; ++nt) {
+                const int first = row0 + mt * 16;
+                const int ha = (first >> head_shift) & (kh - 1);
+                const int hb = ((first + 15) >> head_shift) & (kh - 1);
+                const int c0 = hg * Gm::NT * 8 + nt * 8;
+                const bool nd = kh == 1 || (c0 / G <= max(ha, hb) && (c0 + 7) / G >= min(ha, hb));
+                if (nd) {
+                    need |= 1u << (mt * Gm::NT + nt);
+                    nt_any |= 1u << nt;
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int row = first + gq + (e >= 2 ? 8 : 0);
+                    const int col = head_of(nt, e & 1);
+                    if (kh == 1 || ((row >> head_shift) & (kh - 1)) == col / G)
+                        col_ok |= 1u << ((mt * Gm::NT + nt) * 4 + e);
+                }
+            }
+        }
     }
 
     __device__ __forceinline__ int head_of(int nt, int hc) const {
@@ -282,17 +327,26 @@ struct ConsumerState {
         }
     }
 
+    // ldmatrix address of 16-byte chunk c (of D/8) in the row whose block offset is `row_off`
+    __device__ __forceinline__ uint32_t chunk_addr(uint32_t tile, uint32_t row_off, int c) const {
+        return tile + row_off + static_cast<uint32_t>(c >> 3) * half_stride +
+               ((static_cast<uint32_t>(c & 7) ^ static_cast<uint32_t>(lane & 7)) << 4);
+    }
+
     // One stage: this warp's MT*16 rows of the tile.  `mask` bit r = row r of the tile is valid.
-    // kh > 1: tile rows come in blocks of 2^rb_shift rows cycling over the unit's kh KV heads, and
-    // a score is kept only where the row's KV head is the column's.
+    // Scores outside col_ok (another KV head's rows) are dropped; n-tiles outside `need` skip
+    // their MMAs and, when no m-tile of the stage needs them, their whole softmax update (their
+    // state is unchanged, exactly as if every score were masked).
     __device__ __forceinline__ void consume(uint32_t k_tile, uint32_t v_tile, uint64_t mask,
-                                            float scale_log2, int rb_shift, int kh) {
+                                            float scale_log2) {
         constexpr int kRows = Gm::MT * 16;
         const uint64_t rows_mask = kRows == 64 ? ~0ull : ((1ull << kRows) - 1ull);
         const uint64_t wmask = (mask >> (kg * kRows)) & rows_mask;
         if (wmask == 0) return;               // no valid row: the state is unchanged
         const bool all_valid = wmask == rows_mask;
-        const int row0 = kg * kRows;
+        constexpr uint32_t kAllCols = (Gm::MT * Gm::NT * 4 >= 32) ? 0xffffffffu
+                                                                  : ((1u << (Gm::MT * Gm::NT * 4)) - 1u);
+        const bool all_cols = col_ok == kAllCols;
 
         // S^T[row, head] = sum_d K[row, d] * Q[head, d]
         float s[Gm::MT][Gm::NT][4];
@@ -304,17 +358,18 @@ struct ConsumerState {
                 for (int e = 0; e < 4; ++e) s[mt][nt][e] = 0.f;
 #pragma unroll
         for (int mt = 0; mt < Gm::MT; ++mt) {
-            const int r = row0 + mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
             for (int ks = 0; ks < Gm::KSTEPS; ++ks) {
                 uint32_t a[4];
-                ldmatrix_x4(a, k_tile + tile_offset<Gm::kHalves>(r, 2 * ks + (lane >> 4), rb_shift));
+                ldmatrix_x4(a, chunk_addr(k_tile, k_row_off[mt], 2 * ks + (lane >> 4)));
 #pragma unroll
-                for (int nt = 0; nt < Gm::NT; ++nt) mma_bf16_16816(s[mt][nt], a, qf[ks][nt][0], qf[ks][nt][1]);
+                for (int nt = 0; nt < Gm::NT; ++nt)
+                    if (need & (1u << (mt * Gm::NT + nt)))
+                        mma_bf16_16816(s[mt][nt], a, qf[ks][nt][0], qf[ks][nt][1]);
             }
         }
 
-        // scale into the log2 domain; invalid rows (and other KV heads' rows) -> -inf
+        // scale into the log2 domain; invalid rows and other KV heads' rows -> -inf
 #pragma unroll
         for (int mt = 0; mt < Gm::MT; ++mt)
 #pragma unroll
@@ -324,14 +379,14 @@ struct ConsumerState {
                     float x = s[mt][nt][e] * scale_log2;
                     const int rr = mt * 16 + gq + (e >= 2 ? 8 : 0);
                     if (!all_valid && !((wmask >> rr) & 1ull)) x = -CUDART_INF_F;
-                    if (kh > 1 && (((row0 + rr) >> rb_shift) & (kh - 1)) != col_kv[nt][e & 1])
-                        x = -CUDART_INF_F;
+                    if (!all_cols && !((col_ok >> ((mt * Gm::NT + nt) * 4 + e)) & 1u)) x = -CUDART_INF_F;
                     s[mt][nt][e] = x;
                 }
 
         // online softmax update per head column
 #pragma unroll
-        for (int nt = 0; nt < Gm::NT; ++nt)
+        for (int nt = 0; nt < Gm::NT; ++nt) {
+            if (!((nt_any >> nt) & 1u)) continue;   // no row of this warp reaches these heads
 #pragma unroll
             for (int hc = 0; hc < 2; ++hc) {
                 float mx = -CUDART_INF_F;
@@ -356,6 +411,7 @@ struct ConsumerState {
                     s[mt][nt][hc + 2] = fast_exp2(s[mt][nt][hc + 2] - m_use);
                 }
             }
+        }
 
         // P (rounded to bf16; the sum uses the rounded weights) -> P^T B fragments
         uint32_t pb[Gm::MT][Gm::NT][2];
@@ -363,6 +419,10 @@ struct ConsumerState {
         for (int mt = 0; mt < Gm::MT; ++mt)
 #pragma unroll
             for (int nt = 0; nt < Gm::NT; ++nt) {
+                if (!(need & (1u << (mt * Gm::NT + nt)))) {
+                    pb[mt][nt][0] = pb[mt][nt][1] = 0u;
+                    continue;
+                }
                 const uint32_t r0 = pack_bf16x2(s[mt][nt][0], s[mt][nt][1]);  // row gq
                 const uint32_t r1 = pack_bf16x2(s[mt][nt][2], s[mt][nt][3]);  // row gq + 8
                 l_run[nt][0] += bf16_lo_to_f32(r0) + bf16_lo_to_f32(r1);
@@ -374,7 +434,6 @@ struct ConsumerState {
         // O^T[d, head] += sum_row V[row, d] * P[row, head]
 #pragma unroll
         for (int mt = 0; mt < Gm::MT; ++mt) {
-            const int r = row0 + mt * 16 + (lane & 7) + ((lane >> 4) << 3);
             uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;
             if (!all_valid) {
                 const int k0 = mt * 16 + 2 * qd;
@@ -386,7 +445,7 @@ struct ConsumerState {
 #pragma unroll
             for (int dt = 0; dt < Gm::DT; ++dt) {
                 uint32_t a[4];
-                ldmatrix_x4_trans(a, v_tile + tile_offset<Gm::kHalves>(r, 2 * dt + ((lane >> 3) & 1), rb_shift));
+                ldmatrix_x4_trans(a, chunk_addr(v_tile, v_row_off[mt], 2 * dt + ((lane >> 3) & 1)));
                 if (!all_valid) {   // rows never loaded or past the length may hold NaN
                     a[0] &= keep_lo;
                     a[1] &= keep_lo;
@@ -394,7 +453,9 @@ struct ConsumerState {
                     a[3] &= keep_hi;
                 }
 #pragma unroll
-                for (int nt = 0; nt < Gm::NT; ++nt) mma_bf16_16816(o[dt][nt], a, pb[mt][nt][0], pb[mt][nt][1]);
+                for (int nt = 0; nt < Gm::NT; ++nt)
+                    if (need & (1u << (mt * Gm::NT + nt)))
+                        mma_bf16_16816(o[dt][nt], a, pb[mt][nt][0], pb[mt][nt][1]);
             }
         }
     }
@@ -664,7 +725,7 @@ __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& 
 
 // ------------------------------------------------------------------ the kernel
 template <int VAR, int D, int GP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<VAR>::kThreads, 1)
 decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const Params p) {
     using Gm = Geometry<D, GP>;
@@ -675,7 +736,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(sm.full + s, VAR == kSparse ? 33u : 1u);
+            mbar_init(sm.full + s, VAR == kSparse ? 32u * Roles<VAR>::kProducerWarps + 1u : 1u);
             mbar_init(sm.empty + s, kConsumerWarps);
         }
         mbar_init(sm.group, kConsumerThreads);
@@ -697,7 +758,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     int N = 0, C = 1, t0 = 0, t1 = 0;
     if (VAR == kPaged) {
         const int cap = p.max_pages * p.page_size;
-        for (int b = threadIdx.x; b < p.B; b += kThreads) {
+        for (int b = threadIdx.x; b < p.B; b += Roles<VAR>::kThreads) {
             const unsigned raw = __ldg(p.kv_lens + static_cast<size_t>(b) * p.kv_stride);
             const int len = raw > static_cast<unsigned>(cap) ? cap : static_cast<int>(raw);
             sm.seq_len[b] = len;
@@ -746,12 +807,16 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         t1 = (sp_key0 + sp_nkeys + kTileKeys - 1) / kTileKeys;
     }
 
-    if (warp == kConsumerWarps) {
-        // ================================================================ producer warp
+    if (warp >= kConsumerWarps) {
+        // ================================================================ producer warps
         int it = 0;
         bool ok = true;
         if (VAR == kSparse) {
             const int b = sp_u / p.Hkv;
+            constexpr int NPW = Roles<VAR>::kProducerWarps;
+            constexpr int kRowsPerWarp = kTileKeys / NPW;  // rows of a tile each producer warp copies
+            const int ptid = threadIdx.x - kConsumerThreads;
+            const int pw = ptid >> 5;
             constexpr int CH = D / 8;                     // 16-byte chunks per row
             constexpr int kRowsPerInstr = 32 / (2 * CH);  // K and V of 1 (D=128) or 2 (D=64) rows
             const int sub = lane / (2 * CH);
@@ -763,11 +828,11 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             // every entry outside [0, pool_rows) folded to -1
             int* sidx = sm.seq_prefix;
             const int* selrow = p.sel + static_cast<size_t>(b) * p.width + sp_key0;
-            for (int i = lane; i < sp_nkeys; i += 32) {
+            for (int i = ptid; i < sp_nkeys; i += 32 * NPW) {
                 const int idx = __ldg(selrow + i);
                 sidx[i] = (idx >= 0 && idx < p.pool_rows) ? idx : -1;
             }
-            __syncwarp();
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * NPW) : "memory");   // producer warps only
             for (int t = t0; t < t1 && ok; ++t, ++it) {
                 const int s = it % S;
                 const uint32_t ph = (it / S) & 1;
@@ -781,11 +846,12 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 const uint64_t mask = static_cast<uint64_t>(__ballot_sync(0xffffffffu, v0)) |
                                       (static_cast<uint64_t>(__ballot_sync(0xffffffffu, v1)) << 32);
                 unsigned char* tile = sm.stages + s * Gm::kStageBytes + (isv ? Gm::kTileBytes : 0);
+                const int row_begin = pw * kRowsPerWarp;
                 const __nv_bfloat16* base = pool + static_cast<size_t>(sp_u) * p.pool_rows * D + c * 8;
                 // independent iterations: each lane reads its row's entry from shared memory, so
                 // the unrolled loop keeps several index reads and copies in flight
 #pragma unroll 8
-                for (int rb = 0; rb < kTileKeys; rb += kRowsPerInstr) {
+                for (int rb = row_begin; rb < row_begin + kRowsPerWarp; rb += kRowsPerInstr) {
                     const int r = rb + sub;
                     const int li = l0 + r;
                     const int idx = li < sp_nkeys ? sidx[li] : -1;
@@ -793,9 +859,9 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     const __nv_bfloat16* src = base + static_cast<size_t>(valid ? idx : 0) * D;
                     cp_async_16(tile + tile_offset<Gm::kHalves>(r, c, 6), src, valid ? 16u : 0u);
                 }
-                if (lane == 0) sm.stage_mask[s] = mask;
+                if (ptid == 0) sm.stage_mask[s] = mask;
                 cp_async_arrive_noinc(sm.full + s);
-                if (lane == 0) mbar_arrive(sm.full + s);
+                if (ptid == 0) mbar_arrive(sm.full + s);
             }
             if (!ok) {
                 cp_async_wait_all();
@@ -805,11 +871,13 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         } else {
             // dense / paged: lane 0 issues TMA; paged uses all lanes to fetch block-table entries
             const int P = p.page_size;
+            // paged: a page group is the kh adjacent heads of one page, kh * P contiguous rows;
+            // box_rows = min(kh * P, 64) rows of it per box and half
             const int TK = VAR == kPaged ? p.tile_keys : kTileKeys;   // keys per stage and KV head
-            const int box_rows = VAR == kPaged ? min(P, TK) : kTileKeys;
+            const int box_rows = VAR == kPaged ? min(P * p.kh, kTileKeys) : kTileKeys;
+            const int head_rows = VAR == kPaged ? min(P, TK) : kTileKeys;   // rows per head and page
             const int pages_per_tile = VAR == kPaged ? (P >= TK ? 1 : TK / P) : 1;
             const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * 128u;
-            const uint64_t box_mask = box_rows >= 64 ? ~0ull : ((1ull << box_rows) - 1ull);
             int bt_b = -1, bt_base = -1;   // current batch: slots [bt_base, bt_base + 32) of sequence bt_b
             int bt_cur = -1, bt_nxt = -1;
             for (int t = t0; t < t1 && ok;) {
@@ -863,37 +931,31 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                                 page_ok |= 1u << i;
                         }
                         if (lane == 0) {
-                            // rows of the tile: page i, then KV head hh of the unit, then slot
+                            // rows of the tile: page i (a block of box_rows rows), then KV head hh
+                            // of the unit (head_rows rows each), then slot
                             uint32_t nloaded = 0;
                             uint64_t rows = 0;
                             for (int i = 0; i < pages_per_tile; ++i) {
                                 if (!(page_ok & (1u << i))) continue;
                                 ++nloaded;
-                                const int nv = min(box_rows, U.len - (key0 + i * box_rows));
+                                const int nv = min(head_rows, U.len - (key0 + i * head_rows));
                                 if (nv <= 0) continue;
                                 const uint64_t bits = nv >= 64 ? ~0ull : ((1ull << nv) - 1ull);
                                 for (int hh = 0; hh < p.kh; ++hh)
-                                    rows |= (bits & box_mask) << ((i * p.kh + hh) * box_rows);
+                                    rows |= bits << (i * box_rows + hh * head_rows);
                             }
                             mask = rows;
                             sm.stage_mask[s] = mask;
-                            mbar_arrive_expect_tx(sm.full + s,
-                                                  nloaded * 2u * p.kh * Gm::kHalves * box_bytes);
+                            mbar_arrive_expect_tx(sm.full + s, nloaded * 2u * Gm::kHalves * box_bytes);
+                            const int row_coord = U.g * p.kh * P + row_in_page;
                             for (int i = 0; i < pages_per_tile; ++i) {
                                 if (!(page_ok & (1u << i))) continue;
-                                // blocks i*kh .. i*kh+kh-1 of the tile, halves one after the other
-                                const int dst = i * p.kh * Gm::kHalves * box_rows * 128;
-                                if (p.page_box_nd) {
-                                    const int h0 = U.g * p.kh;
-                                    tma_load_5d(ktile + dst, &tm_k, 0, row_in_page, 0, h0, pages[i], sm.full + s);
-                                    tma_load_5d(vtile + dst, &tm_v, 0, row_in_page, 0, h0, pages[i], sm.full + s);
-                                } else {
+                                const int dst = i * Gm::kHalves * box_rows * 128;   // block i
 #pragma unroll
-                                    for (int h = 0; h < Gm::kHalves; ++h) {
-                                        const int dh = dst + h * box_rows * 128;
-                                        tma_load_3d(ktile + dh, &tm_k, 64 * h, U.g * P + row_in_page, pages[i], sm.full + s);
-                                        tma_load_3d(vtile + dh, &tm_v, 64 * h, U.g * P + row_in_page, pages[i], sm.full + s);
-                                    }
+                                for (int h = 0; h < Gm::kHalves; ++h) {
+                                    const int dh = dst + h * box_rows * 128;
+                                    tma_load_3d(ktile + dh, &tm_k, 64 * h, row_coord, pages[i], sm.full + s);
+                                    tma_load_3d(vtile + dh, &tm_v, 64 * h, row_coord, pages[i], sm.full + s);
                                 }
                             }
                         }
@@ -919,10 +981,11 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
 
     // ==================================================================== consumer warps
-    const int rb_shift = VAR == kPaged ? 31 - __clz(min(p.page_size, p.tile_keys)) : 6;
+    const int rb_shift = VAR == kPaged ? 31 - __clz(min(p.page_size * p.kh, kTileKeys)) : 6;
     const int kh = VAR == kPaged ? p.kh : 1;
+    const int head_shift = VAR == kPaged ? 31 - __clz(p.page_size) : 6;
     ConsumerState<D, GP> cs;
-    cs.init(warp, lane, p.G);
+    cs.init(warp, lane, p.G, kh, rb_shift, head_shift);
     uint32_t gphase = 0;
 
     if (VAR == kPaged) {
@@ -958,7 +1021,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 return;
             }
             const uint32_t ktile = smem_u32(sm.stages + s * Gm::kStageBytes);
-            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2, rb_shift, kh);
+            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2);
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty + s);
         }
@@ -987,7 +1050,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 return;
             }
             const uint32_t ktile = smem_u32(sm.stages + s * Gm::kStageBytes);
-            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2, rb_shift, kh);
+            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2);
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty + s);
         }

@@ -14,6 +14,7 @@ struct Launch {
     CUtensorMap tm_v;
     Params p;
     int grid;
+    int threads;        // block size of the variant
     cudaStream_t stream;
 };
 
@@ -26,7 +27,7 @@ cudaError_t launch_paged(int D, int GP, const Launch& L);
 cudaError_t launch_sparse(int D, int GP, const Launch& L);
 
 // Opts the kernel into `smem` bytes of dynamic shared memory on the current device (once per
-// kernel and device), then launches it.
+// kernel and device), then launches it with L.threads threads per block.
 cudaError_t launch_kernel(const void* kernel, int smem, const Launch& L);
 
 }  // namespace da
