@@ -160,6 +160,8 @@ def parse_overrides(items):
 
 def case_bytes_copied(case):
     """Host->device bytes of one end-to-end step: the buffers the step reads."""
+    if case.kind == "append":
+        return 2 * case.k_new.numel() * 2 + case.slot_mapping.numel() * 8
     if case.kind == "dense":
         live = 2 * case.B * case.Hkv * case.k_len * case.D * 2
         return case.q.numel() * 2 + live
@@ -182,6 +184,12 @@ class HostCopy:
                                               ctypes.c_size_t, ctypes.c_size_t, ctypes.c_size_t,
                                               ctypes.c_int, ctypes.c_void_p]
         c = case
+        if c.kind == "append":
+            self.kn = c.k_new.cpu().pin_memory()
+            self.vn = c.v_new.cpu().pin_memory()
+            self.sm = c.slot_mapping.cpu().pin_memory()
+            self.out = None
+            return
         if c.kind == "dense":
             self.q = c.q.cpu().pin_memory()
             self.k = c.k[:, :, :c.k_len].contiguous().cpu().pin_memory()
@@ -202,6 +210,11 @@ class HostCopy:
     def h2d(self, stream):
         c = self.case
         s = stream.cuda_stream
+        if c.kind == "append":
+            c.k_new.copy_(self.kn, non_blocking=True)
+            c.v_new.copy_(self.vn, non_blocking=True)
+            c.slot_mapping.copy_(self.sm, non_blocking=True)
+            return
         c.q.copy_(self.q, non_blocking=True)
         if c.kind == "dense":
             rows = c.B * c.Hkv
@@ -223,7 +236,8 @@ class HostCopy:
             c.sel.copy_(self.sel, non_blocking=True)
 
     def d2h(self, out):
-        self.out.copy_(out, non_blocking=True)
+        if self.out is not None:      # append: the result is the device cache itself
+            self.out.copy_(out, non_blocking=True)
 
 
 def dist_setup(args):
@@ -300,7 +314,31 @@ def cpu_case(name):
     return c
 
 
+def append_cpu_sample(name: str, budget_s: float):
+    """The oracle's append on the host: rows of the workload written into a host pool sized for
+    them, as many as take about budget_s; returns (bytes of that sample, seconds, threads)."""
+    import oracle
+    cfg = {**W.CONFIGS[name], **OVERRIDES}
+    T, Hkv, D, P = cfg["T"], cfg["Hkv"], cfg["D"], cfg["page_size"]
+    rows = min(T, 512)
+    while True:
+        pages = max(1, 2 * rows // P + 1)
+        c = W.make_append(rows, Hkv, D, P, pages, seed=cfg["seed"])
+        kp = c.k_pool.view(torch.int16).numpy().view(np.uint16).copy()
+        vp = c.v_pool.view(torch.int16).numpy().view(np.uint16).copy()
+        t0 = time.perf_counter()
+        oracle.append_paged(c.k_new, c.v_new, kp, vp, c.slot_mapping.numpy(), inplace=True)
+        secs = time.perf_counter() - t0
+        if secs * 4 > budget_s or rows >= T:
+            return c.algorithmic_bytes(), secs, 1, rows
+        rows = min(T, rows * 4)
+
+
 def cpu_baseline(name: str, budget_s: float = 15.0):
+    if W.CONFIGS[name]["kind"] == "append":
+        nbytes, secs, threads, rows = append_cpu_sample(name, budget_s)
+        return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": threads,
+                "kind": "oracle", "sample": f"{rows} appended rows of {name} in {secs:.3f} s"}
     c = cpu_case(name)
     rows, secs, threads = oracle_sample_run(c, budget_s)
     frac = rows / (c.B * c.Hq)
@@ -314,6 +352,27 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     name = args.workload
+    if W.CONFIGS[name]["kind"] == "append":
+        times = []
+        for i in range(args.warmup + args.steps):
+            nbytes, secs, threads, rows = append_cpu_sample(name, 2.0)
+            if i >= args.warmup:
+                times.append(secs / nbytes)
+        per_byte = float(np.mean(times))
+        cfg = W.CONFIGS[name]
+        total = 2 * 2 * cfg["T"] * cfg["Hkv"] * cfg["D"] * 2 + cfg["T"] * 8
+        gbs = 1.0 / per_byte / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(total * per_byte * 1e3, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16 copy", "data": "synthetic",
+                "config": {"workload": name},
+                "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1,
+                                 "kind": "oracle", "sample": f"{rows} rows per step"},
+                "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
     c = cpu_case(name)
     per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     times = []
@@ -351,10 +410,14 @@ def run_native(args, world, rank, local):
     name = args.workload
     cases = [make_case(name, dev, seed_offset=1000 * rank + k) for k in range(2)]
     c0 = cases[0]
-    var = {"dense": 0, "paged": 1, "sparse": 2}[c0.kind]
-    ws = B_.new_workspace(B_.decode_attn_workspace_size(
-        var, c0.B, c0.Hq, c0.Hkv, c0.D, getattr(c0, "width", 0)), dev)
-    outs = [torch.empty(c.out_shape(), dtype=torch.bfloat16, device=dev) for c in cases]
+    if c0.kind == "append":
+        ws = None
+        outs = [c.k_pool for c in cases]
+    else:
+        var = {"dense": 0, "paged": 1, "sparse": 2}[c0.kind]
+        ws = B_.new_workspace(B_.decode_attn_workspace_size(
+            var, c0.B, c0.Hq, c0.Hkv, c0.D, getattr(c0, "width", 0)), dev)
+        outs = [torch.empty(c.out_shape(), dtype=torch.bfloat16, device=dev) for c in cases]
     stream = torch.cuda.Stream(dev)
     alg = [c.algorithmic_bytes() for c in cases]
 
@@ -396,7 +459,7 @@ def run_native(args, world, rank, local):
     # ---- end to end: pinned host inputs copied in and the output copied back every step
     hc = [HostCopy(c) for c in cases]
     h2d = case_bytes_copied(c0)
-    d2h = outs[0].numel() * 2
+    d2h = 0 if c0.kind == "append" else outs[0].numel() * 2
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(args.steps, 20))

@@ -125,6 +125,61 @@ da_status decode_attn_sparse(const void *q, const void *k_pool, const void *v_po
                              int Hkv, int D, float softmax_scale, void *workspace,
                              size_t workspace_bytes, void *stream);
 
+/*
+ * KV append into the paged cache (reshape_and_cache): the step before decode_attn_paged.
+ * Follows "DflashScratch" (docs.metrale.ai dflash_head), field slot_mapping_dev: row t of k_new /
+ * v_new ([T, Hkv, D], bf16) is written to every KV head of slot s = slot_mapping[t] (i64, device
+ * memory) of the pools [num_pages, Hkv, page_size, D]: page s / page_size, position
+ * s % page_size.  A slot outside [0, num_pages * page_size) (-1 padding or any other) writes
+ * nothing; the slots are read on the device and never validated by a sync.  Two rows naming the
+ * same slot race (one of them wins).  D a multiple of 8, at most 1024; k_new, v_new and the pools
+ * 16-byte aligned, slot_mapping 8-byte aligned.  Enqueues one kernel on `stream`.
+ */
+da_status decode_attn_append_paged(const void *k_new, const void *v_new, void *k_pool,
+                                   void *v_pool, const int64_t *slot_mapping, int64_t T, int Hkv,
+                                   int D, int page_size, int64_t num_pages, void *stream);
+
+/*
+ * KV append into a ring window: the step before decode_attn_sparse.
+ * Follows "AttnV41" (docs.metrale.ai attn_v41), method decode_body: the window ring write at
+ * pos % window, the slot read on the device.  Row b of k_new / v_new ([B, Hkv, D]) is written to
+ * row positions[b] % window (i64, device memory) of sequence b's pools [B, Hkv, pool_rows, D]
+ * (the window occupies rows [0, window)); a negative position writes nothing.
+ * 1 <= window <= pool_rows; alignment as for decode_attn_append_paged.
+ */
+da_status decode_attn_append_ring(const void *k_new, const void *v_new, void *k_pool,
+                                  void *v_pool, const int64_t *positions, int B, int Hkv, int D,
+                                  int64_t pool_rows, int window, void *stream);
+
+/*
+ * The options of a decode-attention region, as "DecodeFlashSpec" (docs.rs
+ * fuel_dispatch::decode_flash) carries them next to q / k / v / k_len: nonzero has_* fields mean
+ * the option is present.
+ */
+typedef struct {
+    int has_alibi;          /* ALiBi slopes [Hq] present */
+    int causal;             /* causal masking requested */
+    int has_window_left;    /* left sliding-window bound present */
+    int has_window_right;   /* right sliding-window bound present */
+    int has_softcap;        /* logit softcap present */
+    float softmax_scale;
+} decode_attn_spec;
+
+/*
+ * Whether these kernels can compute the region (DecodeFlashSpec's gate): ALiBi, either
+ * sliding-window bound or a softcap disqualify it (DA_ERR_UNSUPPORTED: the kernels have no such
+ * parameter, so the caller keeps its decomposed path); causal is accepted and ignored, since one
+ * query row attends the whole live prefix; a null spec or a non-finite scale is
+ * DA_ERR_INVALID_ARGUMENT.  Host only; touches no device.
+ */
+da_status decode_attn_spec_check(const decode_attn_spec *spec);
+
+/* decode_attn_spec_check, then decode_attn_dense with spec->softmax_scale. */
+da_status decode_attn_dense_spec(const decode_attn_spec *spec, const void *q, const void *k,
+                                 const void *v, void *out, int B, int Hq, int Hkv, int D,
+                                 int64_t capacity, int64_t k_len, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
 /* Caps the number of CTAs the dense and paged calls spread their work over (0 = one per SM,
  * the default).  Process-wide; a smaller grid gives every KV head more split segments, which
  * exercises the cross-CTA log-sum-exp merge.  Returns DA_ERR_INVALID_ARGUMENT for a negative

@@ -188,11 +188,18 @@ def dense_range(q, k, v, b: int, h: int, j0: int, j1: int, scale: float):
     return o, lse.value
 
 
-def append_paged(k_new, v_new, k_pool, v_pool, slot_mapping):
+def append_paged(k_new, v_new, k_pool, v_pool, slot_mapping, inplace: bool = False):
     """k_new, v_new [T,Hkv,D]; pools [num_pages,Hkv,page_size,D]; slot_mapping int64 [T].
-    Returns (k_pool', v_pool') as new uint16 arrays; the inputs are not modified."""
+    Returns (k_pool', v_pool') as new uint16 arrays (inplace=True writes into the given uint16
+    pool arrays instead and returns them)."""
     kn, vn = _bits(k_new), _bits(v_new)
-    kp, vp = _bits(k_pool).copy(), _bits(v_pool).copy()
+    if inplace:
+        kp, vp = k_pool, v_pool
+        if not (isinstance(kp, np.ndarray) and kp.dtype == np.uint16 and kp.flags.c_contiguous
+                and isinstance(vp, np.ndarray) and vp.dtype == np.uint16 and vp.flags.c_contiguous):
+            raise TypeError("inplace append needs C-contiguous uint16 pool arrays")
+    else:
+        kp, vp = _bits(k_pool).copy(), _bits(v_pool).copy()
     sm = np.ascontiguousarray(np.asarray(slot_mapping, dtype=np.int64).reshape(-1))
     T = sm.size
     num_pages, Hkv, P, D = kp.shape

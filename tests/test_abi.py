@@ -121,3 +121,54 @@ def test_misc_host_calls(lib):
     assert lib.decode_attn_workspace_size(0, 1, 6, 4, 128, 0) == 0
     assert lib.decode_attn_workspace_size(2, 1, 8, 1, 96, 10) == 0
     assert lib.decode_attn_workspace_size(7, 1, 8, 1, 128, 10) == 0
+
+
+def test_append_rejects(lib):
+    def ap(k=FAKE, sm=FAKE, T=4, Hkv=2, D=128, P=16, npages=8):
+        return lib.decode_attn_append_paged(k, FAKE, FAKE, FAKE, sm, T, Hkv, D, P, npages, None)
+
+    def ar(pos=FAKE, B=2, D=128, R=64, window=16):
+        return lib.decode_attn_append_ring(FAKE, FAKE, FAKE, FAKE, pos, B, 2, D, R, window, None)
+
+    assert ap(k=None) == INVALID
+    assert ap(sm=None) == INVALID
+    assert ap(sm=FAKE + 4) == INVALID          # slot words must be 8-byte aligned
+    assert ap(T=-1) == INVALID
+    assert ap(P=0) == INVALID
+    assert ap(D=100) == UNSUPPORTED
+    assert ap(T=0) == OK                      # nothing to write
+    assert ar(window=0) == INVALID
+    assert ar(window=65) == INVALID           # window larger than the pool
+    assert ar(pos=None) == INVALID
+    assert ar(B=0) == OK
+
+
+class Spec(ctypes.Structure):
+    _fields_ = [("has_alibi", ctypes.c_int), ("causal", ctypes.c_int),
+                ("has_window_left", ctypes.c_int), ("has_window_right", ctypes.c_int),
+                ("has_softcap", ctypes.c_int), ("softmax_scale", ctypes.c_float)]
+
+
+def test_flash_spec_gate(lib):
+    """Which options disqualify the flash arm (tests/golden/flash_spec_gate.json)."""
+    import json
+    rule = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "flash_spec_gate.json")))
+    lib.decode_attn_spec_check.argtypes = [ctypes.POINTER(Spec)]
+    lib.decode_attn_spec_check.restype = ctypes.c_int
+    assert lib.decode_attn_spec_check(ctypes.byref(Spec(softmax_scale=0.125))) == OK
+    for f in rule["accepted_and_ignored"]:
+        s = Spec(softmax_scale=0.125)
+        setattr(s, f, 1)
+        assert lib.decode_attn_spec_check(ctypes.byref(s)) == OK, f
+    for f in rule["disqualify"]:
+        s = Spec(softmax_scale=0.125, causal=1)
+        setattr(s, f, 1)
+        assert lib.decode_attn_spec_check(ctypes.byref(s)) == UNSUPPORTED, f
+    assert lib.decode_attn_spec_check(None) == INVALID
+    assert lib.decode_attn_spec_check(ctypes.byref(Spec(softmax_scale=math.nan))) == INVALID
+    # the spec entry point refuses before touching any (here fake) device pointer
+    lib.decode_attn_dense_spec.restype = ctypes.c_int
+    s = Spec(softmax_scale=0.1, has_softcap=1)
+    assert lib.decode_attn_dense_spec(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 128,
+                                      ctypes.c_int64(16), ctypes.c_int64(8), FAKE,
+                                      ctypes.c_size_t(1 << 20), None) == UNSUPPORTED

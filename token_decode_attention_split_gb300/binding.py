@@ -55,6 +55,10 @@ def load_library() -> ctypes.CDLL:
                                           sz, vp]
         lib.decode_attn_sparse.restype = i
         lib.decode_attn_sparse.argtypes = [vp, vp, vp, vp, i64, vp, i, i, i, i, i, f, vp, sz, vp]
+        lib.decode_attn_append_paged.restype = i
+        lib.decode_attn_append_paged.argtypes = [vp, vp, vp, vp, vp, i64, i, i, i, i64, vp]
+        lib.decode_attn_append_ring.restype = i
+        lib.decode_attn_append_ring.argtypes = [vp, vp, vp, vp, vp, i, i, i, i64, i, vp]
         lib.decode_attn_set_grid_limit.restype = i
         lib.decode_attn_set_grid_limit.argtypes = [i]
         lib.decode_attn_read_device_error.restype = i
@@ -151,6 +155,22 @@ def decode_attn_sparse(q, k_pool, v_pool, out, sel, softmax_scale: float, worksp
     return out
 
 
+def decode_attn_append_paged(k_new, v_new, k_pool, v_pool, slot_mapping, stream=None):
+    """k_new, v_new [T,Hkv,D] bf16; pools [num_pages,Hkv,page_size,D]; slot_mapping int64 [T]."""
+    T, Hkv, D = k_new.shape
+    _check(load_library().decode_attn_append_paged(
+        _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(slot_mapping), T, Hkv, D,
+        k_pool.shape[2], k_pool.shape[0], _stream(stream, k_new.device)), "decode_attn_append_paged")
+
+
+def decode_attn_append_ring(k_new, v_new, k_pool, v_pool, positions, window: int, stream=None):
+    """k_new, v_new [B,Hkv,D] bf16; pools [B,Hkv,pool_rows,D]; positions int64 [B]."""
+    B, Hkv, D = k_new.shape
+    _check(load_library().decode_attn_append_ring(
+        _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(positions), B, Hkv, D,
+        k_pool.shape[2], int(window), _stream(stream, k_new.device)), "decode_attn_append_ring")
+
+
 def run_case(case, out=None, workspace=None, stream=None):
     """Runs one workload object (``workloads.DenseCase`` / ``PagedCase`` / ``SparseCase``) through
     the matching entry point, allocating the output and a zeroed workspace when not given."""
@@ -169,6 +189,10 @@ def run_case(case, out=None, workspace=None, stream=None):
                 DA_VARIANT_PAGED, case.B, case.Hq, case.Hkv, case.D), dev)
         return decode_attn_paged(case.q, case.k_pool, case.v_pool, out, case.block_table,
                                  case.kv_args, case.kv_len_stride, case.scale, workspace, stream)
+    if case.kind == "append":
+        decode_attn_append_paged(case.k_new, case.v_new, case.k_pool, case.v_pool,
+                                 case.slot_mapping, stream)
+        return case.k_pool
     if case.kind == "sparse":
         if workspace is None:
             workspace = new_workspace(decode_attn_workspace_size(

@@ -13,7 +13,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libdecode_attn.so")
-SOURCES = ["api.cu", "kernels_dense.cu", "kernels_paged.cu", "kernels_sparse.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "kernels_dense.cu", "kernels_paged.cu", "kernels_sparse.cu", "noalloc.cu",
+           "append.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

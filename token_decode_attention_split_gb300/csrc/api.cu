@@ -290,6 +290,23 @@ da_status decode_attn_workspace_init(void* workspace, size_t bytes, void* stream
                : DA_ERR_CUDA;
 }
 
+da_status decode_attn_spec_check(const decode_attn_spec* spec) {
+    if (!spec || !std::isfinite(spec->softmax_scale)) return DA_ERR_INVALID_ARGUMENT;
+    if (spec->has_alibi || spec->has_window_left || spec->has_window_right || spec->has_softcap)
+        return DA_ERR_UNSUPPORTED;
+    return DA_OK;   // causal: a single query row attends the whole live prefix anyway
+}
+
+da_status decode_attn_dense_spec(const decode_attn_spec* spec, const void* q, const void* k,
+                                 const void* v, void* out, int B, int Hq, int Hkv, int D,
+                                 int64_t capacity, int64_t k_len, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+    const da_status st = decode_attn_spec_check(spec);
+    if (st != DA_OK) return st;
+    return decode_attn_dense(q, k, v, out, B, Hq, Hkv, D, capacity, k_len, spec->softmax_scale,
+                             workspace, workspace_bytes, stream);
+}
+
 da_status decode_attn_set_grid_limit(int max_ctas) {
     if (max_ctas < 0) return DA_ERR_INVALID_ARGUMENT;
     g_grid_limit.store(max_ctas);

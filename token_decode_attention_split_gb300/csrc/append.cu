@@ -1,0 +1,149 @@
+// KV append: the step before decode attention that writes this step's new K/V rows into the
+// cache the attention kernels read.
+//   decode_attn_append_paged  "DflashScratch" (dflash_head), field slot_mapping_dev: row t goes to
+//                             the paged-cache slot slot_mapping[t] (i64) of every KV head.
+//   decode_attn_append_ring   "AttnV41" (attn_v41), method decode_body: the window ring write at
+//                             pos % window, the position read on the device.
+// Both are plain HBM-bound copies: one warp moves one (row, KV head) of K and of V with 16-byte
+// loads and stores; the slot or position is read on the device and never validated by a sync.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "decode_attn.h"
+#include "ptx.cuh"
+
+namespace {
+
+constexpr int kAppendThreads = 256;   // 8 warps, one (row, KV head) each per step
+
+struct AppendArgs {
+    const uint4* k_new;   // [rows, Hkv, D] as 16-byte chunks
+    const uint4* v_new;
+    uint4* k_pool;
+    uint4* v_pool;
+    const int64_t* where;  // slot per row (paged) or position per sequence (ring)
+    int64_t rows;          // T (paged) or B (ring)
+    int Hkv;
+    int chunks;            // 16-byte chunks per row: D / 8
+    int64_t page_size;     // paged
+    int64_t num_slots;     // paged: num_pages * page_size
+    int64_t pool_rows;     // ring
+    int64_t window;        // ring
+    int ring;
+};
+
+// Destination row (in units of rows of D elements) of (row, KV head g), or -1 to skip.
+__device__ __forceinline__ int64_t dest_row(const AppendArgs& a, int64_t row, int g) {
+    const int64_t w = a.where[row];
+    if (a.ring) {
+        if (w < 0) return -1;
+        return (row * a.Hkv + g) * a.pool_rows + w % a.window;
+    }
+    if (w < 0 || w >= a.num_slots) return -1;
+    const int64_t page = w / a.page_size, off = w - page * a.page_size;
+    return (page * a.Hkv + g) * a.page_size + off;
+}
+
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs a) {
+    da::grid_dependency_wait();
+    da::allow_dependent_launch();
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kAppendThreads / 32);
+    const int64_t total = a.rows * a.Hkv;
+    for (int64_t wi = blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5); wi < total;
+         wi += warps) {
+        const int64_t row = wi / a.Hkv;
+        const int g = static_cast<int>(wi - row * a.Hkv);
+        const int64_t dst = dest_row(a, row, g);
+        if (dst < 0) continue;
+        const int64_t src = (row * a.Hkv + g) * a.chunks;
+        const int64_t dc = dst * a.chunks;
+        for (int c = lane; c < 2 * a.chunks; c += 32) {
+            const bool isv = c >= a.chunks;
+            const int cc = isv ? c - a.chunks : c;
+            const uint4 x = __ldg((isv ? a.v_new : a.k_new) + src + cc);
+            (isv ? a.v_pool : a.k_pool)[dc + cc] = x;
+        }
+    }
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+da_status launch(const AppendArgs& a, void* stream) {
+    const int64_t work = a.rows * a.Hkv;
+    if (work == 0) return DA_OK;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return DA_ERR_CUDA;
+    const int64_t want = (work + kAppendThreads / 32 - 1) / (kAppendThreads / 32);
+    const int grid = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kAppendThreads);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, append_kernel, a) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+da_status check_rows(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                     const int64_t* where, int64_t rows, int Hkv, int D) {
+    if (!k_new || !v_new || !k_pool || !v_pool || !where) return DA_ERR_INVALID_ARGUMENT;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+        !aligned(where, 8))
+        return DA_ERR_INVALID_ARGUMENT;
+    if (rows < 0 || Hkv <= 0 || D <= 0) return DA_ERR_INVALID_ARGUMENT;
+    if (D % 8 != 0 || D > 1024) return DA_ERR_UNSUPPORTED;
+    return DA_OK;
+}
+
+}  // namespace
+
+extern "C" da_status decode_attn_append_paged(const void* k_new, const void* v_new, void* k_pool,
+                                              void* v_pool, const int64_t* slot_mapping, int64_t T,
+                                              int Hkv, int D, int page_size, int64_t num_pages,
+                                              void* stream) {
+    const da_status st = check_rows(k_new, v_new, k_pool, v_pool, slot_mapping, T, Hkv, D);
+    if (st != DA_OK) return st;
+    if (page_size <= 0 || num_pages < 0) return DA_ERR_INVALID_ARGUMENT;
+    AppendArgs a{};
+    a.k_new = static_cast<const uint4*>(k_new);
+    a.v_new = static_cast<const uint4*>(v_new);
+    a.k_pool = static_cast<uint4*>(k_pool);
+    a.v_pool = static_cast<uint4*>(v_pool);
+    a.where = slot_mapping;
+    a.rows = T;
+    a.Hkv = Hkv;
+    a.chunks = D / 8;
+    a.page_size = page_size;
+    a.num_slots = num_pages * page_size;
+    a.ring = 0;
+    return launch(a, stream);
+}
+
+extern "C" da_status decode_attn_append_ring(const void* k_new, const void* v_new, void* k_pool,
+                                             void* v_pool, const int64_t* positions, int B,
+                                             int Hkv, int D, int64_t pool_rows, int window,
+                                             void* stream) {
+    const da_status st = check_rows(k_new, v_new, k_pool, v_pool, positions, B, Hkv, D);
+    if (st != DA_OK) return st;
+    if (window <= 0 || pool_rows < window) return DA_ERR_INVALID_ARGUMENT;
+    AppendArgs a{};
+    a.k_new = static_cast<const uint4*>(k_new);
+    a.v_new = static_cast<const uint4*>(v_new);
+    a.k_pool = static_cast<uint4*>(k_pool);
+    a.v_pool = static_cast<uint4*>(v_pool);
+    a.where = positions;
+    a.rows = B;
+    a.Hkv = Hkv;
+    a.chunks = D / 8;
+    a.pool_rows = pool_rows;
+    a.window = window;
+    a.ring = 1;
+    return launch(a, stream);
+}

@@ -42,6 +42,9 @@ CONFIGS = {
     # sparse, fixed-width int32 selection with trailing -1 pads
     "sparse_selected": dict(kind="sparse", B=32, Hq=64, Hkv=1, D=128, pool_rows=65536, width=2048,
                             window=128, max_pad=512, seed=1005),
+    # KV append into the paged cache (the step before paged decode): a ctx window of new rows
+    "append_paged": dict(kind="append", T=8192, Hkv=8, D=128, page_size=16, num_pages=160000,
+                         seed=1006),
 }
 
 
@@ -163,6 +166,43 @@ class SparseCase:
         return (self.B, self.Hq, 1, self.D)
 
 
+@dataclass
+class AppendCase:
+    k_new: torch.Tensor        # [T, Hkv, D] bf16
+    v_new: torch.Tensor
+    k_pool: torch.Tensor       # [num_pages, Hkv, page_size, D] bf16
+    v_pool: torch.Tensor
+    slot_mapping: torch.Tensor  # [T] int64
+    T: int
+    Hkv: int
+    D: int
+    page_size: int
+    num_pages: int
+    kind: str = "append"
+
+    def algorithmic_bytes(self) -> int:
+        """New rows read + written (K and V, valid slots) + slot words."""
+        valid = int(((self.slot_mapping >= 0) &
+                     (self.slot_mapping < self.num_pages * self.page_size)).sum())
+        return 2 * 2 * valid * self.Hkv * self.D * 2 + self.T * 8
+
+
+def make_append(T, Hkv, D, page_size, num_pages, seed, device="cpu", pad_every=0) -> AppendCase:
+    """T new rows to distinct random slots of a paged pool; with pad_every = n, every n-th slot
+    is -1 (a padding row)."""
+    dev, g, gc = _gens(seed, device)
+    if T > num_pages * page_size:
+        raise ValueError("more rows than slots")
+    slots = torch.randperm(num_pages * page_size, generator=gc)[:T].to(torch.int64)
+    if pad_every:
+        slots[::pad_every] = -1
+    k_new = _normal_bf16((T, Hkv, D), g, dev)
+    v_new = _normal_bf16((T, Hkv, D), g, dev)
+    k_pool = _normal_bf16((num_pages, Hkv, page_size, D), g, dev)
+    v_pool = _normal_bf16((num_pages, Hkv, page_size, D), g, dev)
+    return AppendCase(k_new, v_new, k_pool, v_pool, slots.to(dev), T, Hkv, D, page_size, num_pages)
+
+
 def make_dense(B, Hq, Hkv, D, capacity, k_len, seed, device="cpu", k_scale=1.0,
                poison_tail=False, scale=None) -> DenseCase:
     dev, g, _ = _gens(seed, device)
@@ -264,4 +304,6 @@ def make(name: str, device="cpu", **overrides):
         return make_paged(device=device, **cfg)
     if kind == "sparse":
         return make_sparse(device=device, **cfg)
+    if kind == "append":
+        return make_append(device=device, **cfg)
     raise KeyError(kind)
