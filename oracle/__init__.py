@@ -17,6 +17,9 @@ What each function computes, with the page each follows:
     selection whose -1 entries add nothing.
   * ``dense_range`` -- the same dense definition restricted to rows [j0, j1), returning the
     normalised row and its natural-log log-sum-exp (for the split/merge identity tests).
+  * ``dense_mq`` / ``paged_mq`` -- several query tokens per sequence (q, out [B, Hq, Sq, D]): the
+    Sq new tokens are the last Sq rows of the live prefix; causal token i attends rows
+    [0, len - Sq + i] ("DecodeFlashSpec", q [B,Hq,Sq,D] and field causal; "AttnV41", forward).
   * ``append_paged`` -- "DflashScratch", field slot_mapping_dev (reshape_and_cache): new K/V rows
     scattered to paged-cache slots; ``append_ring`` -- "AttnV41", method decode_body: the ring
     write at pos % window.  Both return updated copies of the pools.
@@ -71,10 +74,14 @@ def _load():
                                       i64p, i64, i]
         lib.oracle_dense_range.argtypes = [u16p, u16p, u16p, i, i, i, i, i64, i, i, i64, i64, d,
                                            f64p, f64p]
+        lib.oracle_dense_mq.argtypes = [u16p, u16p, u16p, f64p, i, i, i, i, i, i, i64, i64, d, i]
+        lib.oracle_paged_mq.argtypes = [u16p, u16p, u16p, f64p, i32p, i64, i64, i64, u32p, i64,
+                                        i, i, i, i, i, i, d, i]
         lib.oracle_append_paged.argtypes = [u16p, u16p, u16p, u16p, i64p, i64, i, i, i64, i64]
         lib.oracle_append_ring.argtypes = [u16p, u16p, u16p, u16p, i64p, i, i, i, i64, i64]
         for f in (lib.oracle_dense, lib.oracle_paged, lib.oracle_sparse, lib.oracle_dense_range,
-                  lib.oracle_append_paged, lib.oracle_append_ring):
+                  lib.oracle_append_paged, lib.oracle_append_ring, lib.oracle_dense_mq,
+                  lib.oracle_paged_mq):
             f.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -226,3 +233,38 @@ def append_ring(k_new, v_new, k_pool, v_pool, positions, window: int):
                                     _ptr(pos, ctypes.c_int64), B, Hkv, D, R, int(window))
     _check(rc, "append_ring")
     return kp, vp
+
+
+def dense_mq(q, k, v, k_len: int, scale: float, causal: bool = True, nthreads: int = 0):
+    """q [B,Hq,Sq,D]; k, v [B,Hkv,capacity,D]; returns fp64 [B,Hq,Sq,D]."""
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    B, Hkv, cap, D = kb.shape
+    if qb.ndim != 4:
+        raise ValueError("q must be [B, Hq, Sq, D]")
+    Hq, Sq = qb.shape[1], qb.shape[2]
+    out = np.zeros((B, Hq, Sq, D), dtype=np.float64)
+    rc = _load().oracle_dense_mq(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                 _ptr(vb, ctypes.c_uint16), _ptr(out, ctypes.c_double), B, Hq, Hkv,
+                                 D, Sq, int(bool(causal)), cap, int(k_len), float(scale),
+                                 int(nthreads))
+    _check(rc, "dense_mq")
+    return out
+
+
+def paged_mq(q, k_pool, v_pool, block_table, kv_lens, scale: float, causal: bool = True,
+             kv_len_stride: int = 1, nthreads: int = 0):
+    """q [B,Hq,Sq,D]; pools [num_pages,Hkv,page_size,D]; returns fp64 [B,Hq,Sq,D]."""
+    qb, kb, vb = _bits(q), _bits(k_pool), _bits(v_pool)
+    num_pages, Hkv, P, D = kb.shape
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    B, max_pages = bt.shape
+    kl = np.ascontiguousarray(np.asarray(kv_lens, dtype=np.uint32).reshape(-1))
+    Hq, Sq = qb.shape[1], qb.shape[2]
+    out = np.zeros((B, Hq, Sq, D), dtype=np.float64)
+    rc = _load().oracle_paged_mq(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                 _ptr(vb, ctypes.c_uint16), _ptr(out, ctypes.c_double),
+                                 _ptr(bt, ctypes.c_int32), max_pages, P, num_pages,
+                                 _ptr(kl, ctypes.c_uint32), int(kv_len_stride), B, Hq, Hkv, D, Sq,
+                                 int(bool(causal)), float(scale), int(nthreads))
+    _check(rc, "paged_mq")
+    return out

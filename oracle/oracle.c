@@ -93,6 +93,8 @@ typedef struct {
     int64_t pool_rows;
     const int32_t *sel;
     int64_t width;
+    /* query tokens per sequence (q, out [B, Hq, Sq, D]) and causal masking inside them */
+    int Sq, causal;
     /* which (b*Hq + h) to compute */
     const int64_t *pairs;
     int64_t npairs;
@@ -106,17 +108,26 @@ typedef struct {
     int tid;
 } worker_t;
 
-/* Builds the attended row list of (b, g) in attended order; returns the row count. */
-static int64_t gather_rows(const job_t *J, int b, int g, int64_t *krow) {
+/* The live length of sequence b (dense: k_len; paged: its kv_len, clamped). */
+static int64_t live_len(const job_t *J, int b) {
+    if (J->variant == VAR_DENSE) return J->k_len;
+    int64_t len = (int64_t)J->kv_lens[(int64_t)b * J->kv_len_stride];
+    const int64_t cap = J->max_pages * J->page_size;
+    return len > cap ? cap : len;
+}
+
+/* Builds the attended row list of (b, g) in attended order, keeping only row positions j < jmax
+ * (dense and paged); returns the row count. */
+static int64_t gather_rows(const job_t *J, int b, int g, int64_t jmax, int64_t *krow) {
     const int64_t D = J->D;
     int64_t n = 0;
     if (J->variant == VAR_DENSE) {
         const int64_t base = ((int64_t)b * J->Hkv + g) * J->capacity;
-        for (int64_t j = 0; j < J->k_len; ++j) krow[n++] = (base + j) * D;
+        const int64_t len = J->k_len < jmax ? J->k_len : jmax;
+        for (int64_t j = 0; j < len; ++j) krow[n++] = (base + j) * D;
     } else if (J->variant == VAR_PAGED) {
-        int64_t len = (int64_t)J->kv_lens[(int64_t)b * J->kv_len_stride];
-        const int64_t cap = J->max_pages * J->page_size;
-        if (len > cap) len = cap;
+        int64_t len = live_len(J, b);
+        if (len > jmax) len = jmax;
         for (int64_t j = 0; j < len; ++j) {
             const int64_t page = J->block_table[(int64_t)b * J->max_pages + j / J->page_size];
             if (page < 0 || page >= J->num_pages) continue;
@@ -150,10 +161,16 @@ static void *worker(void *arg) {
         const int64_t bh = J->pairs ? J->pairs[t] : t;
         const int b = (int)(bh / J->Hq), h = (int)(bh % J->Hq);
         const int g = h / G;
-        const int64_t n = gather_rows(J, b, g, rows);
-        /* K and V share one layout, so the same element offsets address both. */
-        attend_rows(J->q + bh * J->D, J->k, J->v, rows, rows, n, J->D, J->scale,
-                    J->out + bh * J->D, s);
+        for (int i = 0; i < J->Sq; ++i) {
+            /* the Sq new tokens are the last Sq rows of the live prefix: causal token i sees rows
+             * [0, len - Sq + i] */
+            const int64_t jmax = J->causal ? live_len(J, b) - J->Sq + i + 1 : INT64_MAX;
+            const int64_t n = jmax <= 0 ? 0 : gather_rows(J, b, g, jmax, rows);
+            const int64_t row = bh * J->Sq + i;
+            /* K and V share one layout, so the same element offsets address both. */
+            attend_rows(J->q + row * J->D, J->k, J->v, rows, rows, n, J->D, J->scale,
+                        J->out + row * J->D, s);
+        }
     }
     free(rows);
     free(s);
@@ -213,6 +230,7 @@ int oracle_dense(const uint16_t *q, const uint16_t *k, const uint16_t *v, double
     J.capacity = capacity; J.k_len = k_len;
     J.pairs = pairs; J.npairs = npairs; J.nthreads = nthreads;
     J.max_rows = k_len;
+    J.Sq = 1;
     return run_job(&J);
 }
 
@@ -235,6 +253,7 @@ int oracle_paged(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_po
     J.num_pages = num_pages; J.kv_lens = kv_lens; J.kv_len_stride = kv_len_stride;
     J.pairs = pairs; J.npairs = npairs; J.nthreads = nthreads;
     J.max_rows = max_pages * page_size;
+    J.Sq = 1;
     return run_job(&J);
 }
 
@@ -251,6 +270,49 @@ int oracle_sparse(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_p
     J.pool_rows = pool_rows; J.sel = sel; J.width = width;
     J.pairs = pairs; J.npairs = npairs; J.nthreads = nthreads;
     J.max_rows = width;
+    J.Sq = 1;
+    return run_job(&J);
+}
+
+/* Several query tokens per sequence (a multi-token verify step): q, out [B, Hq, Sq, D].  The Sq
+ * new tokens are the last Sq rows of each sequence's live prefix, so with causal != 0 token i
+ * attends rows [0, len - Sq + i] (a token at or before row 0 of the prefix sees nothing: a zero
+ * row); with causal = 0 every token attends the whole prefix [0, len).  Sq = 1 is the single-query
+ * decode above.  "DecodeFlashSpec" (q [B,Hq,Sq,D], field causal), "AttnV41" method forward (m
+ * tokens at start_pos). */
+int oracle_dense_mq(const uint16_t *q, const uint16_t *k, const uint16_t *v, double *out, int B,
+                    int Hq, int Hkv, int D, int Sq, int causal, int64_t capacity, int64_t k_len,
+                    double scale, int nthreads) {
+    if (k_len < 0 || k_len > capacity || Sq < 1) return ORACLE_EINVAL;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.variant = VAR_DENSE;
+    J.q = q; J.k = k; J.v = v; J.out = out;
+    J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.D = D; J.scale = scale;
+    J.capacity = capacity; J.k_len = k_len;
+    J.nthreads = nthreads;
+    J.max_rows = k_len;
+    J.Sq = Sq; J.causal = causal;
+    return run_job(&J);
+}
+
+int oracle_paged_mq(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool, double *out,
+                    const int32_t *block_table, int64_t max_pages, int64_t page_size,
+                    int64_t num_pages, const uint32_t *kv_lens, int64_t kv_len_stride, int B,
+                    int Hq, int Hkv, int D, int Sq, int causal, double scale, int nthreads) {
+    if (!block_table || !kv_lens || max_pages < 0 || page_size <= 0 || num_pages < 0 ||
+        kv_len_stride <= 0 || Sq < 1)
+        return ORACLE_EINVAL;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.variant = VAR_PAGED;
+    J.q = q; J.k = k_pool; J.v = v_pool; J.out = out;
+    J.B = B; J.Hq = Hq; J.Hkv = Hkv; J.D = D; J.scale = scale;
+    J.block_table = block_table; J.max_pages = max_pages; J.page_size = page_size;
+    J.num_pages = num_pages; J.kv_lens = kv_lens; J.kv_len_stride = kv_len_stride;
+    J.nthreads = nthreads;
+    J.max_rows = max_pages * page_size;
+    J.Sq = Sq; J.causal = causal;
     return run_job(&J);
 }
 
