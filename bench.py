@@ -283,9 +283,15 @@ def oracle_sample_run(case_host, budget_s: float):
     rows = int(max(1, min(n, budget_s / per_row)))
     pairs = np.linspace(0, n - 1, rows).round().astype(np.int64)
     pairs = np.unique(pairs)
-    t0 = time.perf_counter()
-    _run_oracle(case_host, pairs, threads)
-    return len(pairs), time.perf_counter() - t0, threads
+    # a sample shorter than the budget is repeated (whole passes) to fill about half of it
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        _run_oracle(case_host, pairs, threads)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s / 2 or passes >= 1000:
+            break
+    return len(pairs) * passes, el, threads
 
 
 def _run_oracle(c, pairs, threads):
@@ -344,8 +350,9 @@ def cpu_baseline(name: str, budget_s: float = 15.0):
     frac = rows / (c.B * c.Hq)
     gbs = c.algorithmic_bytes() * frac / secs / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{rows} of {c.B * c.Hq} (b, h) rows of {name} in {secs:.2f} s; "
-                      f"value = that share of the workload's algorithmic bytes / time"}
+            "sample": f"{rows} (b, h) rows of {name} (of {c.B * c.Hq} per call; repeated passes "
+                      f"when shorter) in {secs:.2f} s; value = the matching share of the "
+                      f"workload's algorithmic bytes / time"}
 
 
 def run_reference(args, world, rank):

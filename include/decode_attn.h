@@ -94,6 +94,20 @@ da_status decode_attn_dense(const void *q, const void *k, const void *v, void *o
                             void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * decode_attn_dense with the live length read on the device.
+ * Follows "DecodeFlashSpec", field k_len: for a persistent (plan-once) decode graph k_len is a
+ * symbol bound to the live length each token; here it is one u32 in device memory (*k_len), read
+ * by the kernel at entry and clamped to capacity, so a captured graph replays for every token
+ * while the caller rewrites that word in place (k_len = 0 writes zeros).  The last tile of each
+ * (b, kv head) may fetch up to 63 rows past the length (inside the capacity buffer); they never
+ * contribute.  Other arguments as for decode_attn_dense; k_len must be 4-byte aligned.
+ */
+da_status decode_attn_dense_device_len(const void *q, const void *k, const void *v, void *out,
+                                       int B, int Hq, int Hkv, int D, int64_t capacity,
+                                       const uint32_t *k_len, float softmax_scale,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Paged decode attention with per-sequence lengths read on the device.
  * Follows "DflashScratch" (docs.metrale.ai dflash_head), field option_b_indirect_args_dev: the
  * kernel reads kv_len of sequence b at entry from kv_lens[b * kv_len_stride]; stride 3 reads

@@ -172,3 +172,13 @@ def test_flash_spec_gate(lib):
     assert lib.decode_attn_dense_spec(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 128,
                                       ctypes.c_int64(16), ctypes.c_int64(8), FAKE,
                                       ctypes.c_size_t(1 << 20), None) == UNSUPPORTED
+
+
+def test_dense_device_len_rejects(lib):
+    lib.decode_attn_dense_device_len.restype = ctypes.c_int
+    call = lambda kl, cap=16: lib.decode_attn_dense_device_len(
+        FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 128, ctypes.c_int64(cap), kl, ctypes.c_float(0.1), FAKE,
+        ctypes.c_size_t(1 << 20), None)
+    assert call(None) == INVALID
+    assert call(FAKE + 2) == INVALID        # the length word must be 4-byte aligned
+    assert call(FAKE, cap=0) == INVALID

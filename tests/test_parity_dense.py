@@ -124,3 +124,39 @@ def test_dense_named_workloads(name):
 
 def test_no_device_error_recorded():
     assert B_.decode_attn_read_device_error() == 0
+
+
+def _dev_len_call(c, k_len_word, out=None, ws=None, stream=None):
+    out = torch.empty(c.out_shape(), dtype=torch.bfloat16, device=DEV) if out is None else out
+    ws = B_.new_workspace(B_.decode_attn_workspace_size(0, c.B, c.Hq, c.Hkv, c.D), DEV) if ws is None else ws
+    return B_.decode_attn_dense_device_len(c.q, c.k, c.v, out, k_len_word, c.scale, ws, stream)
+
+
+@pytest.mark.parametrize("n", [0, 1, 63, 64, 65, 700, 1000, 5000])
+def test_device_len_matches_oracle(n):
+    """The live length read from device memory ("DecodeFlashSpec", k_len as a symbol bound each
+    token), clamped to the capacity of 1000 rows."""
+    c = W.make_dense(2, 32, 4, 128, 1000, 1000, seed=90, device=DEV, k_scale=2.0)
+    word = torch.tensor([n], dtype=torch.int32, device=DEV)
+    out = _dev_len_call(c, word)
+    ref_case = W.DenseCase(c.q, c.k, c.v, min(n, 1000), c.scale, c.B, c.Hq, c.Hkv, c.D, 1000)
+    assert_close(out_f64(out), oracle_for(ref_case), f"device k_len {n}")
+
+
+def test_device_len_graph_replay_follows_the_length_word():
+    c = W.make_dense(3, 16, 2, 128, 2048, 2048, seed=91, device=DEV)
+    word = torch.tensor([100], dtype=torch.int32, device=DEV)
+    out = torch.empty(c.out_shape(), dtype=torch.bfloat16, device=DEV)
+    ws = B_.new_workspace(B_.decode_attn_workspace_size(0, c.B, c.Hq, c.Hkv, c.D), DEV)
+    _dev_len_call(c, word, out, ws)           # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=s):
+        _dev_len_call(c, word, out, ws, s)
+    for n in (1, 777, 2048, 64, 0):
+        word.fill_(n)
+        g.replay()
+        torch.cuda.synchronize()
+        ref_case = W.DenseCase(c.q, c.k, c.v, n, c.scale, c.B, c.Hq, c.Hkv, c.D, 2048)
+        assert_close(out_f64(out), oracle_for(ref_case), f"replay with k_len {n}")

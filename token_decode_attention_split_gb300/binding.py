@@ -50,6 +50,9 @@ def load_library() -> ctypes.CDLL:
         lib.decode_attn_workspace_init.argtypes = [vp, sz, vp]
         lib.decode_attn_dense.restype = i
         lib.decode_attn_dense.argtypes = [vp, vp, vp, vp, i, i, i, i, i64, i64, f, vp, sz, vp]
+        lib.decode_attn_dense_device_len.restype = i
+        lib.decode_attn_dense_device_len.argtypes = [vp, vp, vp, vp, i, i, i, i, i64, vp, f, vp, sz,
+                                                     vp]
         lib.decode_attn_paged.restype = i
         lib.decode_attn_paged.argtypes = [vp, vp, vp, vp, vp, i, i, i64, vp, i, i, i, i, i, f, vp,
                                           sz, vp]
@@ -130,6 +133,19 @@ def decode_attn_dense(q, k, v, out, k_len: int, softmax_scale: float, workspace,
     return out
 
 
+def decode_attn_dense_device_len(q, k, v, out, k_len_dev, softmax_scale: float, workspace,
+                                 stream=None):
+    """As decode_attn_dense, with the live length read on the device from k_len_dev (a one-word
+    int32 CUDA tensor holding the u32 length)."""
+    B, Hq, D = _dims_q(q)
+    Hkv, cap = k.shape[1], k.shape[2]
+    _check(load_library().decode_attn_dense_device_len(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, D, cap, _ptr(k_len_dev),
+        float(softmax_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream, q.device)), "decode_attn_dense_device_len")
+    return out
+
+
 def decode_attn_paged(q, k_pool, v_pool, out, block_table, kv_lens, kv_len_stride: int,
                       softmax_scale: float, workspace, stream=None):
     """Pools [num_pages,Hkv,page_size,D] bf16; block_table int32 [B,max_pages]; kv_lens int32
@@ -174,6 +190,10 @@ def decode_attn_append_ring(k_new, v_new, k_pool, v_pool, positions, window: int
 def run_case(case, out=None, workspace=None, stream=None):
     """Runs one workload object (``workloads.DenseCase`` / ``PagedCase`` / ``SparseCase``) through
     the matching entry point, allocating the output and a zeroed workspace when not given."""
+    if case.kind == "append":
+        decode_attn_append_paged(case.k_new, case.v_new, case.k_pool, case.v_pool,
+                                 case.slot_mapping, stream)
+        return case.k_pool
     dev = case.q.device
     if out is None:
         out = torch.empty(case.out_shape(), dtype=torch.bfloat16, device=dev)
@@ -189,10 +209,6 @@ def run_case(case, out=None, workspace=None, stream=None):
                 DA_VARIANT_PAGED, case.B, case.Hq, case.Hkv, case.D), dev)
         return decode_attn_paged(case.q, case.k_pool, case.v_pool, out, case.block_table,
                                  case.kv_args, case.kv_len_stride, case.scale, workspace, stream)
-    if case.kind == "append":
-        decode_attn_append_paged(case.k_new, case.v_new, case.k_pool, case.v_pool,
-                                 case.slot_mapping, stream)
-        return case.k_pool
     if case.kind == "sparse":
         if workspace is None:
             workspace = new_workspace(decode_attn_workspace_size(

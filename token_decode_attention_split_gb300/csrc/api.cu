@@ -327,17 +327,26 @@ da_status decode_attn_read_device_error(uint32_t* code) {
     return DA_OK;
 }
 
-da_status decode_attn_dense(const void* q, const void* k, const void* v, void* out, int B, int Hq,
-                            int Hkv, int D, int64_t capacity, int64_t k_len, float softmax_scale,
-                            void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Dense call with the length either known on the host (k_len_dev == nullptr) or read by the
+// kernel from device memory (then k_len is ignored and capacity bounds everything).
+da_status run_dense(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                    int D, int64_t capacity, int64_t k_len, const uint32_t* k_len_dev,
+                    float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
     da_status st = check_common(q, out, B, Hq, Hkv, D, softmax_scale, workspace);
     if (st != DA_OK) return st;
     if (!k || !v || !aligned(k, 16) || !aligned(v, 16)) return DA_ERR_INVALID_ARGUMENT;
-    if (capacity < 1 || k_len < 0 || k_len > capacity) return DA_ERR_INVALID_ARGUMENT;
+    if (capacity < 1) return DA_ERR_INVALID_ARGUMENT;
+    if (!k_len_dev && (k_len < 0 || k_len > capacity)) return DA_ERR_INVALID_ARGUMENT;
+    if (k_len_dev && !aligned(k_len_dev, 4)) return DA_ERR_INVALID_ARGUMENT;
     if (capacity >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
     const long long units = static_cast<long long>(B) * Hkv;
-    const long long tiles = (k_len + kTileKeys - 1) / kTileKeys;
-    if (units * tiles >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
+    const long long rows = k_len_dev ? capacity : k_len;      // most rows a call can attend
+    const long long tiles = (rows + kTileKeys - 1) / kTileKeys;
+    if (units * ((capacity + kTileKeys - 1) / kTileKeys) >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (B == 0) return DA_OK;
     const int dev = current_device();
@@ -347,22 +356,47 @@ da_status decode_attn_dense(const void* q, const void* k, const void* v, void* o
     const int G = Hq / Hkv, GP = padded_group(G);
     const WsLayout w = ws_layout(units, units + sms, G, D);
     if (workspace_bytes < w.total) return DA_ERR_WORKSPACE_TOO_SMALL;
-    if (k_len == 0) return zero_output(out, B, Hq, D, cs);
+    if (!k_len_dev && k_len == 0) return zero_output(out, B, Hq, D, cs);
 
     Launch L{};
     const cuuint64_t row_bytes = static_cast<cuuint64_t>(D) * 2;
-    if (!encode_3d(&L.tm_k, k, D, k_len, units, row_bytes, row_bytes * capacity, kTileKeys) ||
-        !encode_3d(&L.tm_v, v, D, k_len, units, row_bytes, row_bytes * capacity, kTileKeys))
+    // rows past the live length lie outside the descriptor when the host knows it, so they are
+    // never read; with a device-resident length the descriptor spans the capacity and the last
+    // tile's rows past the length are fetched but masked
+    if (!encode_3d(&L.tm_k, k, D, rows, units, row_bytes, row_bytes * capacity, kTileKeys) ||
+        !encode_3d(&L.tm_v, v, D, rows, units, row_bytes, row_bytes * capacity, kTileKeys))
         return DA_ERR_CUDA;
     L.p = base_params(q, out, B, Hq, Hkv, softmax_scale, device_error_ptr(dev));
     bind_workspace(L.p, workspace, w);
-    L.p.k_len = static_cast<int>(k_len);
+    L.p.k_len = static_cast<int>(rows);
     L.p.dense_tiles = static_cast<int>(tiles);
-    const long long N = units * tiles;
-    L.grid = static_cast<int>(std::min<long long>(persistent_ctas(dev), N));
+    L.p.k_len_dev = reinterpret_cast<const unsigned*>(k_len_dev);
+    L.p.capacity = static_cast<int>(capacity);
+    L.grid = static_cast<int>(k_len_dev ? persistent_ctas(dev)
+                                        : std::min<long long>(persistent_ctas(dev), units * tiles));
     L.stream = cs;
     L.threads = Roles<kDense>::kThreads;
     return launch_dense(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+da_status decode_attn_dense(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                            int Hkv, int D, int64_t capacity, int64_t k_len, float softmax_scale,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+    return run_dense(q, k, v, out, B, Hq, Hkv, D, capacity, k_len, nullptr, softmax_scale,
+                     workspace, workspace_bytes, stream);
+}
+
+da_status decode_attn_dense_device_len(const void* q, const void* k, const void* v, void* out,
+                                       int B, int Hq, int Hkv, int D, int64_t capacity,
+                                       const uint32_t* k_len, float softmax_scale, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+    if (!k_len) return DA_ERR_INVALID_ARGUMENT;
+    return run_dense(q, k, v, out, B, Hq, Hkv, D, capacity, 0, k_len, softmax_scale, workspace,
+                     workspace_bytes, stream);
 }
 
 da_status decode_attn_paged(const void* q, const void* k_pool, const void* v_pool, void* out,

@@ -98,6 +98,8 @@ struct Params {
     // dense
     int k_len;
     int dense_tiles;          // ceil(k_len / 64)
+    const unsigned* k_len_dev;  // if set, k_len is read here on the device (clamped to capacity)
+    int capacity;
     // paged
     const int* block_table;
     int max_pages, page_size, num_pages;
@@ -194,13 +196,13 @@ __device__ __forceinline__ int tile_owner(int t, int N, int C) {
     return static_cast<int>((static_cast<long long>(t + 1) * C + N - 1) / N) - 1;
 }
 
-__device__ __forceinline__ Unit locate_dense(const Params& p, int t) {
+__device__ __forceinline__ Unit locate_dense(const Params& p, int t, int k_len, int tiles) {
     Unit U;
-    U.nt = p.dense_tiles;
+    U.nt = tiles;
     U.u = t / U.nt;
     U.b = U.u / p.Hkv;
     U.g = U.u - U.b * p.Hkv;
-    U.len = p.k_len;
+    U.len = k_len;
     U.base = U.u * U.nt;
     U.hq0 = U.b * p.Hq + U.g * p.G;
     U.nh = p.G;
@@ -783,9 +785,16 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
     __syncthreads();
 
+    // dense: the live length, given on the host or read here from device memory
+    int dlen = p.k_len, dtiles = p.dense_tiles;
+    if (VAR == kDense && p.k_len_dev != nullptr) {
+        const unsigned raw = *p.k_len_dev;
+        dlen = raw > static_cast<unsigned>(p.capacity) ? p.capacity : static_cast<int>(raw);
+        dtiles = (dlen + kTileKeys - 1) / kTileKeys;
+    }
     if (VAR == kDense) {
-        N = p.B * p.Hkv * p.dense_tiles;
-        C = gridDim.x;
+        N = p.B * p.Hkv * dtiles;
+        C = min(static_cast<int>(gridDim.x), N);
     } else if (VAR == kPaged) {
         N = sm.seq_prefix[p.B] * (p.Hkv / p.kh);
         C = min(static_cast<int>(gridDim.x), N);
@@ -881,7 +890,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             int bt_b = -1, bt_base = -1;   // current batch: slots [bt_base, bt_base + 32) of sequence bt_b
             int bt_cur = -1, bt_nxt = -1;
             for (int t = t0; t < t1 && ok;) {
-                const Unit U = VAR == kDense ? locate_dense(p, t) : locate_paged(p, sm, t);
+                const Unit U = VAR == kDense ? locate_dense(p, t, dlen, dtiles) : locate_paged(p, sm, t);
                 const int tend = min(t1, U.base + U.nt);
                 const int npages_seq = VAR == kPaged ? (U.len + P - 1) / P : 0;
                 for (; t < tend; ++t, ++it) {
@@ -988,6 +997,13 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     cs.init(warp, lane, p.G, kh, rb_shift, head_shift);
     uint32_t gphase = 0;
 
+    if (VAR == kDense && dlen == 0) {
+        // a device-resident length of 0: every row is a zero row (null-row convention)
+        for (size_t idx = static_cast<size_t>(blockIdx.x) * kConsumerThreads + threadIdx.x;
+             idx < static_cast<size_t>(p.B) * p.Hq * D;
+             idx += static_cast<size_t>(gridDim.x) * kConsumerThreads)
+            p.out[idx] = __float2bfloat16_rn(0.f);
+    }
     if (VAR == kPaged) {
         // sequences with no rows get zero rows (null-row convention)
         for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
@@ -1032,7 +1048,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 
     Unit U;
     if (t0 < t1) {
-        U = VAR == kDense ? locate_dense(p, t0) : locate_paged(p, sm, t0);
+        U = VAR == kDense ? locate_dense(p, t0, dlen, dtiles) : locate_paged(p, sm, t0);
         cs.load_q(p, U.hq0, U.nh);
     }
     for (int t = t0; t < t1;) {
@@ -1057,7 +1073,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         // the next segment's Q rows are fetched now so their latency hides behind the finish
         Unit next = U;
         if (t < t1) {
-            next = VAR == kDense ? locate_dense(p, t) : locate_paged(p, sm, t);
+            next = VAR == kDense ? locate_dense(p, t, dlen, dtiles) : locate_paged(p, sm, t);
             cs.load_q(p, next.hq0, next.nh);
         }
         if (!finish_segment<D, GP>(p, sm, cs, U, whole, static_cast<int>(blockIdx.x) + U.u,
