@@ -124,6 +124,28 @@ da_status decode_attn_paged(const void *q, const void *k_pool, const void *v_poo
                             size_t workspace_bytes, void *stream);
 
 /*
+ * Several query tokens per sequence (a multi-token verify step): q, out [B, Hq, Sq, D].
+ * Follows "DecodeFlashSpec" (q is [B, Hq, Sq, D]; field causal) and "AttnV41" method forward
+ * (attention for m tokens at start_pos): the Sq new tokens are the last Sq rows of each
+ * sequence's live prefix, so with causal != 0 token i attends rows [0, len - Sq + i] (a token with
+ * no row gets a zero output row); with causal == 0 every token attends [0, len).  len is k_len
+ * (dense) or the device-resident kv_len (paged).  Sq = 1 is decode_attn_dense /
+ * decode_attn_paged.  Requires (Hq / Hkv) * Sq <= 64.  Workspace: decode_attn_workspace_size()
+ * with Hq * Sq in place of Hq.  Other arguments as for the single-token calls.
+ */
+da_status decode_attn_dense_mq(const void *q, const void *k, const void *v, void *out, int B,
+                               int Hq, int Hkv, int D, int Sq, int causal, int64_t capacity,
+                               int64_t k_len, float softmax_scale, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+da_status decode_attn_paged_mq(const void *q, const void *k_pool, const void *v_pool, void *out,
+                               const int32_t *block_table, int max_pages_per_seq, int page_size,
+                               int64_t num_pages, const uint32_t *kv_lens, int kv_len_stride,
+                               int B, int Hq, int Hkv, int D, int Sq, int causal,
+                               float softmax_scale, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/*
  * Sparse decode attention over a fixed-width selection.
  * Follows "AttnV41" (docs.metrale.ai attn_v41), methods decode_fixed_topk and decode_prep: each
  * sequence's selection lists pool rows (window slots, then the shared index selection, then -1

@@ -182,3 +182,12 @@ def test_dense_device_len_rejects(lib):
     assert call(None) == INVALID
     assert call(FAKE + 2) == INVALID        # the length word must be 4-byte aligned
     assert call(FAKE, cap=0) == INVALID
+
+
+def test_multitoken_rejects(lib):
+    lib.decode_attn_dense_mq.restype = ctypes.c_int
+    call = lambda Hq, Hkv, Sq: lib.decode_attn_dense_mq(
+        FAKE, FAKE, FAKE, FAKE, 1, Hq, Hkv, 128, Sq, 1, ctypes.c_int64(64), ctypes.c_int64(32),
+        ctypes.c_float(0.1), FAKE, ctypes.c_size_t(1 << 20), None)
+    assert call(8, 2, 0) == INVALID          # no query token
+    assert call(64, 2, 3) == UNSUPPORTED     # 32 heads x 3 tokens > 64 columns per unit

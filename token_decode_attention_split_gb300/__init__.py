@@ -9,7 +9,8 @@ _BINDING_NAMES = (
     "decode_attn_sparse", "decode_attn_workspace_size", "decode_attn_workspace_init",
     "decode_attn_set_grid_limit", "decode_attn_read_device_error", "library_path",
     "load_library", "new_workspace", "run_case", "decode_attn_append_paged",
-    "decode_attn_append_ring", "decode_attn_dense_device_len",
+    "decode_attn_append_ring", "decode_attn_dense_device_len", "decode_attn_dense_mq",
+    "decode_attn_paged_mq",
     "DA_VARIANT_DENSE", "DA_VARIANT_PAGED", "DA_VARIANT_SPARSE",
 )
 

@@ -56,6 +56,12 @@ def load_library() -> ctypes.CDLL:
         lib.decode_attn_paged.restype = i
         lib.decode_attn_paged.argtypes = [vp, vp, vp, vp, vp, i, i, i64, vp, i, i, i, i, i, f, vp,
                                           sz, vp]
+        lib.decode_attn_dense_mq.restype = i
+        lib.decode_attn_dense_mq.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i64, i64, f, vp, sz,
+                                             vp]
+        lib.decode_attn_paged_mq.restype = i
+        lib.decode_attn_paged_mq.argtypes = [vp, vp, vp, vp, vp, i, i, i64, vp, i, i, i, i, i, i,
+                                             i, f, vp, sz, vp]
         lib.decode_attn_sparse.restype = i
         lib.decode_attn_sparse.argtypes = [vp, vp, vp, vp, i64, vp, i, i, i, i, i, f, vp, sz, vp]
         lib.decode_attn_append_paged.restype = i
@@ -157,6 +163,32 @@ def decode_attn_paged(q, k_pool, v_pool, out, block_table, kv_lens, kv_len_strid
         num_pages, _ptr(kv_lens), int(kv_len_stride), B, Hq, Hkv, D, float(softmax_scale),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream, q.device)),
         "decode_attn_paged")
+    return out
+
+
+def decode_attn_dense_mq(q, k, v, out, k_len: int, causal: bool, softmax_scale: float, workspace,
+                         stream=None):
+    """q, out [B,Hq,Sq,D]; k, v [B,Hkv,capacity,D]: Sq query tokens per sequence."""
+    B, Hq, Sq, D = q.shape
+    Hkv, cap = k.shape[1], k.shape[2]
+    _check(load_library().decode_attn_dense_mq(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, D, Sq, int(bool(causal)), cap,
+        int(k_len), float(softmax_scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream, q.device)),
+        "decode_attn_dense_mq")
+    return out
+
+
+def decode_attn_paged_mq(q, k_pool, v_pool, out, block_table, kv_lens, kv_len_stride: int,
+                         causal: bool, softmax_scale: float, workspace, stream=None):
+    """q, out [B,Hq,Sq,D]; pools and lengths as for decode_attn_paged."""
+    B, Hq, Sq, D = q.shape
+    num_pages, Hkv, P = k_pool.shape[0], k_pool.shape[1], k_pool.shape[2]
+    _check(load_library().decode_attn_paged_mq(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(out), _ptr(block_table), block_table.shape[1], P,
+        num_pages, _ptr(kv_lens), int(kv_len_stride), B, Hq, Hkv, D, Sq, int(bool(causal)),
+        float(softmax_scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream, q.device)), "decode_attn_paged_mq")
     return out
 
 

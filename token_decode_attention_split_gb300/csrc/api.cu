@@ -125,6 +125,8 @@ Params base_params(const void* q, void* out, int B, int Hq, int Hkv, float scale
     p.seg_heads = p.G;
     p.kh = 1;
     p.tile_keys = kTileKeys;
+    p.sq = 1;
+    p.causal = 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = err;
     return p;
@@ -335,9 +337,12 @@ namespace {
 // kernel from device memory (then k_len is ignored and capacity bounds everything).
 da_status run_dense(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
                     int D, int64_t capacity, int64_t k_len, const uint32_t* k_len_dev,
-                    float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+                    float softmax_scale, void* workspace, size_t workspace_bytes, void* stream,
+                    int sq = 1, int causal = 0) {
     da_status st = check_common(q, out, B, Hq, Hkv, D, softmax_scale, workspace);
     if (st != DA_OK) return st;
+    if (sq < 1) return DA_ERR_INVALID_ARGUMENT;
+    if (padded_group((Hq / Hkv) * sq) == 0) return DA_ERR_UNSUPPORTED;
     if (!k || !v || !aligned(k, 16) || !aligned(v, 16)) return DA_ERR_INVALID_ARGUMENT;
     if (capacity < 1) return DA_ERR_INVALID_ARGUMENT;
     if (!k_len_dev && (k_len < 0 || k_len > capacity)) return DA_ERR_INVALID_ARGUMENT;
@@ -353,10 +358,10 @@ da_status run_dense(const void* q, const void* k, const void* v, void* out, int 
     if (dev < 0) return DA_ERR_CUDA;
     const int sms = sm_count(dev);
     if (sms <= 0) return DA_ERR_CUDA;
-    const int G = Hq / Hkv, GP = padded_group(G);
-    const WsLayout w = ws_layout(units, units + sms, G, D);
+    const int G = Hq / Hkv, GP = padded_group(G * sq);
+    const WsLayout w = ws_layout(units, units + sms, G * sq, D);
     if (workspace_bytes < w.total) return DA_ERR_WORKSPACE_TOO_SMALL;
-    if (!k_len_dev && k_len == 0) return zero_output(out, B, Hq, D, cs);
+    if (!k_len_dev && k_len == 0) return zero_output(out, B, Hq * sq, D, cs);
 
     Launch L{};
     const cuuint64_t row_bytes = static_cast<cuuint64_t>(D) * 2;
@@ -372,6 +377,9 @@ da_status run_dense(const void* q, const void* k, const void* v, void* out, int 
     L.p.dense_tiles = static_cast<int>(tiles);
     L.p.k_len_dev = reinterpret_cast<const unsigned*>(k_len_dev);
     L.p.capacity = static_cast<int>(capacity);
+    L.p.sq = sq;
+    L.p.causal = causal ? 1 : 0;
+    L.p.seg_heads = G * sq;
     L.grid = static_cast<int>(k_len_dev ? persistent_ctas(dev)
                                         : std::min<long long>(persistent_ctas(dev), units * tiles));
     L.stream = cs;
@@ -399,13 +407,19 @@ da_status decode_attn_dense_device_len(const void* q, const void* k, const void*
                      workspace_bytes, stream);
 }
 
-da_status decode_attn_paged(const void* q, const void* k_pool, const void* v_pool, void* out,
-                            const int32_t* block_table, int max_pages_per_seq, int page_size,
-                            int64_t num_pages, const uint32_t* kv_lens, int kv_len_stride, int B,
-                            int Hq, int Hkv, int D, float softmax_scale, void* workspace,
-                            size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+da_status run_paged(const void* q, const void* k_pool, const void* v_pool, void* out,
+                    const int32_t* block_table, int max_pages_per_seq, int page_size,
+                    int64_t num_pages, const uint32_t* kv_lens, int kv_len_stride, int B, int Hq,
+                    int Hkv, int D, float softmax_scale, void* workspace, size_t workspace_bytes,
+                    void* stream, int sq, int causal) {
     da_status st = check_common(q, out, B, Hq, Hkv, D, softmax_scale, workspace);
     if (st != DA_OK) return st;
+    if (sq < 1) return DA_ERR_INVALID_ARGUMENT;
+    if (padded_group((Hq / Hkv) * sq) == 0) return DA_ERR_UNSUPPORTED;
     if (!k_pool || !v_pool || !aligned(k_pool, 16) || !aligned(v_pool, 16)) return DA_ERR_INVALID_ARGUMENT;
     if (!block_table || !kv_lens || !aligned(block_table, 4) || !aligned(kv_lens, 4))
         return DA_ERR_INVALID_ARGUMENT;
@@ -431,16 +445,16 @@ da_status decode_attn_paged(const void* q, const void* k_pool, const void* v_poo
     const cuuint64_t page_bytes = row_bytes * page_size * Hkv;
     // Pools viewed as [num_pages][Hkv * page_size rows][D]; a box is min(kh * page_size, 64)
     // rows of one page (kh adjacent heads) by one 64-column half.
-    const int kh = paged_kv_heads(Hkv, G, page_size);
+    const int kh = paged_kv_heads(Hkv, G * sq, page_size);
     const cuuint32_t rows = static_cast<cuuint32_t>(std::min(kh * page_size, kTileKeys));
     if (!encode_3d(&L.tm_k, k_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
                    row_bytes, page_bytes, rows) ||
         !encode_3d(&L.tm_v, v_pool, D, static_cast<cuuint64_t>(Hkv) * page_size, num_pages,
                    row_bytes, page_bytes, rows))
         return DA_ERR_CUDA;
-    const int GP = padded_group(kh * G);
+    const int GP = padded_group(kh * G * sq);
     const long long punits = units / kh;
-    const WsLayout w = ws_layout(punits, punits + sms, kh * G, D);
+    const WsLayout w = ws_layout(punits, punits + sms, kh * G * sq, D);
     if (workspace_bytes < w.total) return DA_ERR_WORKSPACE_TOO_SMALL;
     L.p = base_params(q, out, B, Hq, Hkv, softmax_scale, device_error_ptr(dev));
     bind_workspace(L.p, workspace, w);
@@ -452,11 +466,46 @@ da_status decode_attn_paged(const void* q, const void* k_pool, const void* v_poo
     L.p.kv_stride = kv_len_stride;
     L.p.kh = kh;
     L.p.tile_keys = kTileKeys / kh;
-    L.p.seg_heads = kh * G;
+    L.p.seg_heads = kh * G * sq;
+    L.p.sq = sq;
+    L.p.causal = causal ? 1 : 0;
     L.grid = persistent_ctas(dev);
     L.stream = cs;
     L.threads = Roles<kPaged>::kThreads;
     return launch_paged(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+da_status decode_attn_paged(const void* q, const void* k_pool, const void* v_pool, void* out,
+                            const int32_t* block_table, int max_pages_per_seq, int page_size,
+                            int64_t num_pages, const uint32_t* kv_lens, int kv_len_stride, int B,
+                            int Hq, int Hkv, int D, float softmax_scale, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    return run_paged(q, k_pool, v_pool, out, block_table, max_pages_per_seq, page_size, num_pages,
+                     kv_lens, kv_len_stride, B, Hq, Hkv, D, softmax_scale, workspace,
+                     workspace_bytes, stream, 1, 0);
+}
+
+da_status decode_attn_paged_mq(const void* q, const void* k_pool, const void* v_pool, void* out,
+                               const int32_t* block_table, int max_pages_per_seq, int page_size,
+                               int64_t num_pages, const uint32_t* kv_lens, int kv_len_stride,
+                               int B, int Hq, int Hkv, int D, int Sq, int causal,
+                               float softmax_scale, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+    return run_paged(q, k_pool, v_pool, out, block_table, max_pages_per_seq, page_size, num_pages,
+                     kv_lens, kv_len_stride, B, Hq, Hkv, D, softmax_scale, workspace,
+                     workspace_bytes, stream, Sq, causal);
+}
+
+da_status decode_attn_dense_mq(const void* q, const void* k, const void* v, void* out, int B,
+                               int Hq, int Hkv, int D, int Sq, int causal, int64_t capacity,
+                               int64_t k_len, float softmax_scale, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    return run_dense(q, k, v, out, B, Hq, Hkv, D, capacity, k_len, nullptr, softmax_scale,
+                     workspace, workspace_bytes, stream, Sq, causal);
 }
 
 da_status decode_attn_sparse(const void* q, const void* k_pool, const void* v_pool, void* out,

@@ -105,6 +105,8 @@ struct Params {
     int max_pages, page_size, num_pages;
     int kh;                   // KV heads per unit (paged; 1 otherwise), a power of two
     int tile_keys;            // keys per stage and KV head: 64 / kh
+    int sq;                   // query tokens per sequence (q, out [B, Hq, sq, D]); 1 = decode
+    int causal;               // sq > 1: token i attends rows [0, len - sq + i]
     const unsigned* kv_lens;
     int kv_stride;
     // sparse
@@ -204,8 +206,8 @@ __device__ __forceinline__ Unit locate_dense(const Params& p, int t, int k_len, 
     U.g = U.u - U.b * p.Hkv;
     U.len = k_len;
     U.base = U.u * U.nt;
-    U.hq0 = U.b * p.Hq + U.g * p.G;
-    U.nh = p.G;
+    U.hq0 = (U.b * p.Hq + U.g * p.G) * p.sq;
+    U.nh = p.G * p.sq;
     U.cu = U.u;
     return U;
 }
@@ -227,8 +229,8 @@ __device__ __forceinline__ Unit locate_paged(const Params& p, const SmemPtrs& sm
     U.u = U.b * upb + U.g;
     U.len = sm.seq_len[lo];
     U.base = sm.seq_prefix[lo] * upb + U.g * U.nt;
-    U.hq0 = U.b * p.Hq + U.g * p.kh * p.G;
-    U.nh = p.kh * p.G;
+    U.hq0 = (U.b * p.Hq + U.g * p.kh * p.G) * p.sq;
+    U.nh = p.kh * p.G * p.sq;
     U.cu = U.u;
     return U;
 }
@@ -249,13 +251,22 @@ struct ConsumerState {
     uint32_t col_ok;                      // bit (mt*NT + nt)*4 + e: score element may be kept
     uint32_t need;                        // bit mt*NT + nt: the n-tile can see the m-tile's rows
     uint32_t nt_any;                      // bit nt: some m-tile of this warp needs n-tile nt
+    int col_tok[Gm::NT][2];               // query token (0..sq-1) of each of this thread's columns
+    int rbs, hsh;                         // rb_shift and head_shift (row -> key offset)
 
     // rb_shift: log2 of the rows per block of the tile layout; kh > 1 (paged units of kh KV
     // heads): row r of the tile belongs to the unit's KV head (r >> head_shift) & (kh - 1), and a
-    // query-head column c to KV head c / G.
+    // query column c to KV head c / G (G: query columns per KV head, heads * tokens) and to
+    // token c % sq.
     __device__ __forceinline__ void init(int warp, int lane_, int G, int kh, int rb_shift,
-                                         int head_shift) {
+                                         int head_shift, int sq) {
         lane = lane_;
+        rbs = rb_shift;
+        hsh = head_shift;
+#pragma unroll
+        for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) col_tok[nt][hc] = head_of(nt, hc) % sq;
         hg = warp % Gm::HS;
         kg = warp / Gm::HS;
         gq = lane >> 2;
@@ -339,8 +350,12 @@ struct ConsumerState {
     // Scores outside col_ok (another KV head's rows) are dropped; n-tiles outside `need` skip
     // their MMAs and, when no m-tile of the stage needs them, their whole softmax update (their
     // state is unchanged, exactly as if every score were masked).
+    // Causal (several query tokens): the tile's row r holds key key0 + off(r) of the unit; a
+    // score is dropped where that key lies past causal_base + token.  Only tiles reaching a key
+    // >= causal_from (the first key some token cannot see) pay for the test.
     __device__ __forceinline__ void consume(uint32_t k_tile, uint32_t v_tile, uint64_t mask,
-                                            float scale_log2) {
+                                            float scale_log2, int key0, int causal_base,
+                                            int causal_from) {
         constexpr int kRows = Gm::MT * 16;
         const uint64_t rows_mask = kRows == 64 ? ~0ull : ((1ull << kRows) - 1ull);
         const uint64_t wmask = (mask >> (kg * kRows)) & rows_mask;
@@ -381,6 +396,11 @@ struct ConsumerState {
                     float x = s[mt][nt][e] * scale_log2;
                     const int rr = mt * 16 + gq + (e >= 2 ? 8 : 0);
                     if (!all_valid && !((wmask >> rr) & 1ull)) x = -CUDART_INF_F;
+                    if (key0 + kTileKeys > causal_from) {
+                        const int r = kg * kRows + rr;
+                        const int key = key0 + ((r >> rbs) << hsh) + (r & ((1 << hsh) - 1));
+                        if (key > causal_base + col_tok[nt][e & 1]) x = -CUDART_INF_F;
+                    }
                     if (!all_cols && !((col_ok >> ((mt * Gm::NT + nt) * 4 + e)) & 1u)) x = -CUDART_INF_F;
                     s[mt][nt][e] = x;
                 }
@@ -994,13 +1014,13 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int kh = VAR == kPaged ? p.kh : 1;
     const int head_shift = VAR == kPaged ? 31 - __clz(p.page_size) : 6;
     ConsumerState<D, GP> cs;
-    cs.init(warp, lane, p.G, kh, rb_shift, head_shift);
+    cs.init(warp, lane, p.G * p.sq, kh, rb_shift, head_shift, p.sq);
     uint32_t gphase = 0;
 
     if (VAR == kDense && dlen == 0) {
         // a device-resident length of 0: every row is a zero row (null-row convention)
         for (size_t idx = static_cast<size_t>(blockIdx.x) * kConsumerThreads + threadIdx.x;
-             idx < static_cast<size_t>(p.B) * p.Hq * D;
+             idx < static_cast<size_t>(p.B) * p.Hq * p.sq * D;
              idx += static_cast<size_t>(gridDim.x) * kConsumerThreads)
             p.out[idx] = __float2bfloat16_rn(0.f);
     }
@@ -1008,8 +1028,8 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         // sequences with no rows get zero rows (null-row convention)
         for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
             if (sm.seq_len[b] != 0) continue;
-            for (int idx = threadIdx.x; idx < p.Hq * D; idx += kConsumerThreads)
-                p.out[static_cast<size_t>(b) * p.Hq * D + idx] = __float2bfloat16_rn(0.f);
+            for (int idx = threadIdx.x; idx < p.Hq * p.sq * D; idx += kConsumerThreads)
+                p.out[static_cast<size_t>(b) * p.Hq * p.sq * D + idx] = __float2bfloat16_rn(0.f);
         }
     }
 
@@ -1037,7 +1057,8 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 return;
             }
             const uint32_t ktile = smem_u32(sm.stages + s * Gm::kStageBytes);
-            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2);
+            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2, 0, 0,
+                       0x7fffffff);
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty + s);
         }
@@ -1056,6 +1077,9 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         const bool whole = (t == U.base) && (tend == U.base + U.nt);
         const int c_first = tile_owner(U.base, N, C);
         const int c_last = tile_owner(U.base + U.nt - 1, N, C);
+        const int tk = VAR == kPaged ? p.tile_keys : kTileKeys;
+        const int causal_base = U.len - p.sq;
+        const int causal_from = p.causal ? causal_base + 1 : 0x7fffffff;
         cs.reset();
         for (; t < tend; ++t, ++it) {
             const int s = it % S;
@@ -1066,7 +1090,8 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 return;
             }
             const uint32_t ktile = smem_u32(sm.stages + s * Gm::kStageBytes);
-            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2);
+            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2,
+                       (t - U.base) * tk, causal_base, causal_from);
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty + s);
         }
