@@ -263,14 +263,14 @@ struct ConsumerState {
         lane = lane_;
         rbs = rb_shift;
         hsh = head_shift;
-#pragma unroll
-        for (int nt = 0; nt < Gm::NT; ++nt)
-#pragma unroll
-            for (int hc = 0; hc < 2; ++hc) col_tok[nt][hc] = head_of(nt, hc) % sq;
         hg = warp % Gm::HS;
         kg = warp / Gm::HS;
         gq = lane >> 2;
         qd = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < Gm::NT; ++nt)
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) col_tok[nt][hc] = head_of(nt, hc) % sq;
         const int row0 = kg * Gm::MT * 16;
         half_stride = 1u << (rb_shift + 7);
         auto block_row = [&](int r) -> uint32_t {
