@@ -31,6 +31,7 @@ import torch  # noqa: E402
 from token_decode_attention_split_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and µs per call"
+NOMINAL_HBM_GBS = 8000.0     # the ~8 TB/s nominal HBM3e figure of a GB300, context only
 DEFAULT_WORKLOAD = "dense_batched"
 KERNEL_SOURCES = ["token_decode_attention_split_gb300/csrc/decode_kernel.cuh",
                   "token_decode_attention_split_gb300/csrc/ptx.cuh"]
@@ -497,6 +498,7 @@ def run_native(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
         "us_per_call": round(step_ms * 1e3, 2),
         "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "pct_of_nominal_8tbs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": name + ("" if not OVERRIDES else " (overridden)"),

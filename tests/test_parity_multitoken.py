@@ -55,6 +55,7 @@ def test_dense_multitoken_matches_oracle(B, Hq, Hkv, D, cap, k_len, Sq, causal, 
     (4, 32, 8, 128, 16, 400, 4, True),          # four KV heads per unit
     (3, 16, 2, 128, 64, 120, 2, True),          # one KV head per unit, 64-row pages
     (3, 32, 8, 128, 16, 400, 2, False),
+    (3, 16, 8, 128, 16, 400, 2, True),          # G = 2: each warp holds one KV head's columns
 ])
 def test_paged_multitoken_matches_oracle(B, Hq, Hkv, D, P, npages, Sq, causal):
     c = W.make_paged(B, Hq, Hkv, D, P, npages, 1, 600, seed=130 + P, device=DEV)

@@ -236,10 +236,18 @@ __device__ __forceinline__ Unit locate_paged(const Params& p, const SmemPtrs& sm
 }
 
 // ------------------------------------------------------------------ consumer warp state
-template <int D, int GP>
+// GW: query columns a warp holds in registers.  GW == GP: every warp holds all of the unit's
+// columns.  GW == 8 < GP (paged units of kh > 1 KV heads with pages of >= 16 rows): the 16 rows
+// of each warp belong to one KV head, so the warp holds only that head's <= 8 columns, starting
+// at unit column col0; the merge slots stay GP columns wide and the warp marks the others empty.
+template <int D, int GP, int GW = GP>
 struct ConsumerState {
-    using Gm = Geometry<D, GP>;
+    using Gm = Geometry<D, GW>;
+    static_assert(GW == GP || (GW == 8 && Gm::KS == kConsumerWarps &&
+                               Geometry<D, GP>::KS == kConsumerWarps),
+                  "warp-per-head columns need one 16-row m-tile per warp");
     int lane, hg, kg, gq, qd;
+    int col0;                             // first unit column held by this warp
     uint32_t qf[Gm::KSTEPS][Gm::NT][2];   // Q^T as mma B fragments
     float o[Gm::DT][Gm::NT][4];           // O^T accumulator fragments
     float m_run[Gm::NT][2];               // running max (log2 domain) of heads 2qd, 2qd+1
@@ -267,6 +275,7 @@ struct ConsumerState {
         kg = warp / Gm::HS;
         gq = lane >> 2;
         qd = lane & 3;
+        col0 = GW == GP ? 0 : (((kg * 16) >> head_shift) & (kh - 1)) * G;
 #pragma unroll
         for (int nt = 0; nt < Gm::NT; ++nt)
 #pragma unroll
@@ -289,7 +298,7 @@ struct ConsumerState {
                 const int first = row0 + mt * 16;
                 const int ha = (first >> head_shift) & (kh - 1);
                 const int hb = ((first + 15) >> head_shift) & (kh - 1);
-                const int c0 = hg * Gm::NT * 8 + nt * 8;
+                const int c0 = col0 + hg * Gm::NT * 8 + nt * 8;
                 const bool nd = kh == 1 || (c0 / G <= max(ha, hb) && (c0 + 7) / G >= min(ha, hb));
                 if (nd) {
                     need |= 1u << (mt * Gm::NT + nt);
@@ -307,14 +316,14 @@ struct ConsumerState {
     }
 
     __device__ __forceinline__ int head_of(int nt, int hc) const {
-        return hg * Gm::NT * 8 + nt * 8 + 2 * qd + hc;
+        return col0 + hg * Gm::NT * 8 + nt * 8 + 2 * qd + hc;
     }
 
     // Q rows hq0 .. hq0 + nh - 1 as B fragments (heads past nh are zero)
     __device__ __forceinline__ void load_q(const Params& p, int hq0, int nh) {
 #pragma unroll
         for (int nt = 0; nt < Gm::NT; ++nt) {
-            const int head = hg * Gm::NT * 8 + nt * 8 + gq;
+            const int head = col0 + hg * Gm::NT * 8 + nt * 8 + gq;
             const bool ok = head < nh;
             const __nv_bfloat16* row = p.q + (static_cast<size_t>(hq0) + (ok ? head : 0)) * D;
             const uint32_t* row32 = reinterpret_cast<const uint32_t*>(row);
@@ -482,8 +491,13 @@ struct ConsumerState {
         }
     }
 
-    // Writes this warp's (m, l, O) for its heads into merge slot kg.
+    // Writes this warp's (m, l, O) for its heads into merge slot kg (with GW < GP the slot's
+    // other columns are marked empty first).
     __device__ __forceinline__ void stash(const SmemPtrs& sm) {
+        if (GW != GP) {
+            for (int c = lane; c < GP; c += 32) sm.merge_m[kg * GP + c] = -CUDART_INF_F;
+            __syncwarp();
+        }
 #pragma unroll
         for (int nt = 0; nt < Gm::NT; ++nt)
 #pragma unroll
@@ -493,6 +507,7 @@ struct ConsumerState {
                 l += __shfl_xor_sync(0xffffffffu, l, 8);
                 l += __shfl_xor_sync(0xffffffffu, l, 16);
                 const int head = head_of(nt, hc);
+                if (GW != GP && head >= GP) continue;   // past the unit's last column
                 const int slot = kg * GP + head;
                 if (gq == 0) {
                     sm.merge_m[slot] = m_run[nt][hc];
@@ -688,9 +703,9 @@ __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, 
 
 // Finishes one segment of unit U: merges the key-split warps, then either stores the output or
 // publishes a partial and, in the CTA that completes the unit, merges all partials.
-template <int D, int GP>
+template <int D, int GP, class CS>
 __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& sm,
-                                               ConsumerState<D, GP>& cs, const Unit& U,
+                                               CS& cs, const Unit& U,
                                                bool whole, int seg, int first_seg, int nseg,
                                                uint32_t& gphase) {
     using Gm = Geometry<D, GP>;
@@ -746,7 +761,7 @@ __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& 
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int VAR, int D, int GP>
+template <int VAR, int D, int GP, int GW = GP>
 __global__ void __launch_bounds__(Roles<VAR>::kThreads, 1)
 decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const Params p) {
@@ -1013,7 +1028,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int rb_shift = VAR == kPaged ? 31 - __clz(min(p.page_size * p.kh, kTileKeys)) : 6;
     const int kh = VAR == kPaged ? p.kh : 1;
     const int head_shift = VAR == kPaged ? 31 - __clz(p.page_size) : 6;
-    ConsumerState<D, GP> cs;
+    ConsumerState<D, GP, GW> cs;
     cs.init(warp, lane, p.G * p.sq, kh, rb_shift, head_shift, p.sq);
     uint32_t gphase = 0;
 
