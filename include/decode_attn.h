@@ -224,8 +224,19 @@ da_status decode_attn_set_grid_limit(int max_ctas);
 
 /* Reads and clears the device error word of the current device (synchronises the device).
  * A kernel whose bounded wait on a pipeline barrier timed out (about one second) stops its
- * work, records a nonzero code here and returns instead of hanging; 0 means no such event. */
+ * work, records a nonzero code here and returns instead of hanging; 0 means no such event.
+ * Codes: 1 a consumer's wait for a filled stage, 2 a producer's wait for a free stage, 3 the
+ * consumer-group barrier, 4 the producer's drain of its own copies after an abort, 5 the check
+ * below.  The first code recorded stays until it is read. */
 da_status decode_attn_read_device_error(uint32_t *code);
+
+/* A check of the failure path (packed_fused_kda_decode's fail-closed convention carried to the
+ * device): enqueues one small kernel whose thread waits, with the bounded wait the decode
+ * pipelines use, on a barrier that nothing completes; after limit_us microseconds the wait gives
+ * up, code 5 is recorded in the device error word and the kernel returns.  The context stays
+ * usable.  1 <= limit_us <= 1000000, else DA_ERR_INVALID_ARGUMENT.  The pages have no such
+ * call; it exists so that a caller (and the tests) can see a timed-out wait surface as an error. */
+da_status decode_attn_check_wait_timeout(uint32_t limit_us, void *stream);
 
 /* Bytes of the library-owned device scratch that decode_attn_dense_noalloc uses: 4 MiB, present
  * on every GPU that loads the library until the process exits. */

@@ -117,6 +117,8 @@ def test_misc_host_calls(lib):
     assert lib.decode_attn_workspace_init(None, 0, None) == OK
     assert lib.decode_attn_workspace_init(None, 16, None) == INVALID
     assert lib.decode_attn_read_device_error(None) == INVALID
+    assert lib.decode_attn_check_wait_timeout(0, None) == INVALID
+    assert lib.decode_attn_check_wait_timeout(1000001, None) == INVALID
     # sizes the calls would reject have no workspace size
     assert lib.decode_attn_workspace_size(0, 1, 6, 4, 128, 0) == 0
     assert lib.decode_attn_workspace_size(2, 1, 8, 1, 96, 10) == 0

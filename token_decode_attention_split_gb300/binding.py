@@ -72,6 +72,8 @@ def load_library() -> ctypes.CDLL:
         lib.decode_attn_set_grid_limit.argtypes = [i]
         lib.decode_attn_read_device_error.restype = i
         lib.decode_attn_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        lib.decode_attn_check_wait_timeout.restype = i
+        lib.decode_attn_check_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         _lib = lib
         return lib
 
@@ -120,6 +122,13 @@ def decode_attn_read_device_error() -> int:
     _check(load_library().decode_attn_read_device_error(ctypes.byref(code)),
            "decode_attn_read_device_error")
     return int(code.value)
+
+
+def decode_attn_check_wait_timeout(limit_us: int, stream=None, device="cuda"):
+    """Enqueues the bounded-wait check: a wait that nothing completes gives up after limit_us
+    and records code 5 in the device error word (read it with decode_attn_read_device_error)."""
+    _check(load_library().decode_attn_check_wait_timeout(int(limit_us), _stream(stream, device)),
+           "decode_attn_check_wait_timeout")
 
 
 def _dims_q(q):

@@ -329,6 +329,18 @@ da_status decode_attn_read_device_error(uint32_t* code) {
     return DA_OK;
 }
 
+da_status decode_attn_check_wait_timeout(uint32_t limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 1000000) return DA_ERR_INVALID_ARGUMENT;
+    const int dev = current_device();
+    if (dev < 0) return DA_ERR_CUDA;
+    unsigned* ptr = device_error_ptr(dev);
+    if (!ptr) return DA_ERR_CUDA;
+    return launch_wait_check(ptr, static_cast<uint64_t>(limit_us) * 1000ull,
+                             static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? DA_OK
+               : DA_ERR_CUDA;
+}
+
 }  // extern "C"
 
 namespace {

@@ -59,7 +59,8 @@ constexpr int kMaxPagedBatch = 1024;
 constexpr int kSmemBudget = 232448;           // opt-in dynamic shared memory per block
 
 enum : int { kDense = 0, kPaged = 1, kSparse = 2 };
-enum : uint32_t { kErrWaitFull = 1, kErrWaitEmpty = 2, kErrWaitGroup = 3, kErrDrain = 4 };
+enum : uint32_t { kErrWaitFull = 1, kErrWaitEmpty = 2, kErrWaitGroup = 3, kErrDrain = 4,
+                  kErrWaitCheck = 5 };
 
 template <int D, int GP>
 struct Geometry {

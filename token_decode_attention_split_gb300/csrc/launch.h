@@ -28,6 +28,10 @@ cudaError_t launch_dense(int D, int GP, const Launch& L);
 cudaError_t launch_paged(int D, int GP, bool warp_head, const Launch& L);
 cudaError_t launch_sparse(int D, int GP, const Launch& L);
 
+// One 32-thread block whose bounded wait on a never-completed barrier times out after limit_ns
+// and records kErrWaitCheck in *err.
+cudaError_t launch_wait_check(unsigned* err, uint64_t limit_ns, cudaStream_t stream);
+
 // Opts the kernel into `smem` bytes of dynamic shared memory on the current device (once per
 // kernel and device), then launches it with L.threads threads per block.
 cudaError_t launch_kernel(const void* kernel, int smem, const Launch& L);
