@@ -504,6 +504,7 @@ def run_native(args, world, rank, local):
         "config": {"workload": name + ("" if not OVERRIDES else " (overridden)"),
                    **{k: v for k, v in {**W.CONFIGS[name], **OVERRIDES}.items() if k != "seed"},
                    "algorithmic_bytes_per_call": int(bytes_step),
+                   "algorithmic_bytes_per_copy": [int(a) for a in alg],
                    "l2": "inputs larger than L2; two input copies alternated",
                    "parallelism": f"replicas x{world}"},
         "e2e": {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
