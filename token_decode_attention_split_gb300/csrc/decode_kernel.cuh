@@ -919,6 +919,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             // paged: a page group is the kh adjacent heads of one page, kh * P contiguous rows;
             // box_rows = min(kh * P, 64) rows of it per box and half
             const int TK = VAR == kPaged ? p.tile_keys : kTileKeys;   // keys per stage and KV head
+            const int page_shift = VAR == kPaged ? 31 - __clz(P) : 0;
             const int box_rows = VAR == kPaged ? min(P * p.kh, kTileKeys) : kTileKeys;
             const int head_rows = VAR == kPaged ? min(P, TK) : kTileKeys;   // rows per head and page
             const int pages_per_tile = VAR == kPaged ? (P >= TK ? 1 : TK / P) : 1;
@@ -950,7 +951,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                             }
                         }
                     } else {
-                        const int slot0 = key0 / P;
+                        const int slot0 = key0 >> page_shift;   // page size: a power of two
                         const int want = slot0 & ~31;
                         if (U.b != bt_b || want != bt_base) {
                             const int* row = p.block_table + static_cast<size_t>(U.b) * p.max_pages;
@@ -965,23 +966,27 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                             const int sn = want + 32 + lane;
                             bt_nxt = sn < npages_seq ? __ldg(row + sn) : -1;
                         }
-                        const int row_in_page = P > TK ? key0 % P : 0;
+                        const int row_in_page = P > TK ? (key0 & (P - 1)) : 0;
                         uint32_t page_ok = 0;
                         int pages[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
-                            pages[i] = __shfl_sync(0xffffffffu, bt_cur, (slot0 - bt_base + i) & 31);
-                            if (i < pages_per_tile && slot0 + i < npages_seq && pages[i] >= 0 &&
-                                pages[i] < p.num_pages)
-                                page_ok |= 1u << i;
+                            if (i < pages_per_tile) {   // warp-uniform
+                                pages[i] = __shfl_sync(0xffffffffu, bt_cur, (slot0 - bt_base + i) & 31);
+                                if (slot0 + i < npages_seq && pages[i] >= 0 && pages[i] < p.num_pages)
+                                    page_ok |= 1u << i;
+                            }
                         }
+                        const uint32_t all_pages = (1u << pages_per_tile) - 1u;
                         if (lane == 0) {
                             // rows of the tile: page i (a block of box_rows rows), then KV head hh
-                            // of the unit (head_rows rows each), then slot
-                            uint32_t nloaded = 0;
-                            uint64_t rows = 0;
-                            for (int i = 0; i < pages_per_tile; ++i) {
-                                if (!(page_ok & (1u << i))) continue;
+                            // of the unit (head_rows rows each), then slot.  A tile inside the
+                            // length whose pages are all in range has every row valid.
+                            const bool full = page_ok == all_pages && key0 + TK <= U.len;
+                            uint32_t nloaded = full ? static_cast<uint32_t>(pages_per_tile) : 0u;
+                            uint64_t rows = full ? ~0ull : 0ull;
+                            for (int i = 0; i < (full ? 0 : pages_per_tile); ++i) {
+                                if (!(page_ok & (1u << i))) continue;   // page_ok only: no pages[i]
                                 ++nloaded;
                                 const int nv = min(head_rows, U.len - (key0 + i * head_rows));
                                 if (nv <= 0) continue;
@@ -993,8 +998,10 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                             sm.stage_mask[s] = mask;
                             mbar_arrive_expect_tx(sm.full + s, nloaded * 2u * Gm::kHalves * box_bytes);
                             const int row_coord = U.g * p.kh * P + row_in_page;
-                            for (int i = 0; i < pages_per_tile; ++i) {
-                                if (!(page_ok & (1u << i))) continue;
+                            // constant trip count: pages[] stays in registers
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                if (!(page_ok & (1u << i))) continue;   // also every i >= pages_per_tile
                                 const int dst = i * Gm::kHalves * box_rows * 128;   // block i
 #pragma unroll
                                 for (int h = 0; h < Gm::kHalves; ++h) {
