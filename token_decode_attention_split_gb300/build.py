@@ -13,8 +13,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libdecode_attn.so")
-SOURCES = ["api.cu", "kernels_dense.cu", "kernels_paged.cu", "kernels_sparse.cu", "noalloc.cu",
-           "append.cu", "wait_check.cu"]
+SOURCES = ["api.cu", "kernels_dense.cu", "kernels_paged.cu", "kernels_paged_multi.cu",
+           "kernels_sparse.cu", "noalloc.cu", "append.cu", "wait_check.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

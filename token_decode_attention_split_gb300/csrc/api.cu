@@ -487,7 +487,9 @@ da_status run_paged(const void* q, const void* k_pool, const void* v_pool, void*
     // Each consumer warp's 16 rows lie in one KV head when pages hold >= 16 rows; with <= 8
     // query columns per KV head the warp then needs only that head's columns.
     const bool warp_head = kh > 1 && page_size >= 16 && G * sq <= 8 && GP == 16;
-    return launch_paged(D, GP, warp_head, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+    const cudaError_t e = kh == 1 ? launch_paged_single(D, GP, L)
+                                  : launch_paged_multi(D, GP, warp_head, L);
+    return e == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
 }  // namespace

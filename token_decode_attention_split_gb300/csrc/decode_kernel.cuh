@@ -45,11 +45,13 @@ namespace da {
 constexpr int kTileKeys = 64;                 // K/V rows per pipeline stage
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-// Producer warps per CTA: one TMA-issuing warp for dense and paged; the sparse gather issues
-// 16-byte cp.async copies, and one warp cannot keep enough of them in flight, so it gets four.
+// Producer warps per CTA: one TMA-issuing warp for dense; two for paged, which take alternate
+// tiles (the block-table lookup makes a paged tile's issue path longer than a dense one); the
+// sparse gather issues 16-byte cp.async copies, and one warp cannot keep enough of them in
+// flight, so it gets four that share every tile.
 template <int VAR>
 struct Roles {
-    static constexpr int kProducerWarps = VAR == 2 ? 4 : 1;
+    static constexpr int kProducerWarps = VAR == 2 ? 4 : VAR == 1 ? 2 : 1;
     static constexpr int kThreads = kConsumerThreads + 32 * kProducerWarps;
 };
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -241,12 +243,21 @@ __device__ __forceinline__ Unit locate_paged(const Params& p, const SmemPtrs& sm
 // columns.  GW == 8 < GP (paged units of kh > 1 KV heads with pages of >= 16 rows): the 16 rows
 // of each warp belong to one KV head, so the warp holds only that head's <= 8 columns, starting
 // at unit column col0; the merge slots stay GP columns wide and the warp marks the others empty.
-template <int D, int GP, int GW = GP>
+// MULTI: a unit spans several KV heads (paged, kh > 1), so the column and n-tile masks depend on
+// the lane and are computed at run time; otherwise every mask is a compile-time constant, which
+// leaves the MMAs of consume() unguarded straight-line code.
+template <int D, int GP, int GW = GP, bool MULTI = false>
 struct ConsumerState {
     using Gm = Geometry<D, GW>;
-    static_assert(GW == GP || (GW == 8 && Gm::KS == kConsumerWarps &&
+    static_assert(GW == GP || (GW == 8 && MULTI && Gm::KS == kConsumerWarps &&
                                Geometry<D, GP>::KS == kConsumerWarps),
                   "warp-per-head columns need one 16-row m-tile per warp");
+    static constexpr uint32_t kAllNeed = (Gm::MT * Gm::NT >= 32) ? 0xffffffffu
+                                                                 : ((1u << (Gm::MT * Gm::NT)) - 1u);
+    static constexpr uint32_t kAllNt = (1u << Gm::NT) - 1u;
+    static constexpr uint32_t kAllCols = (Gm::MT * Gm::NT * 4 >= 32)
+                                             ? 0xffffffffu
+                                             : ((1u << (Gm::MT * Gm::NT * 4)) - 1u);
     int lane, hg, kg, gq, qd;
     int col0;                             // first unit column held by this warp
     uint32_t qf[Gm::KSTEPS][Gm::NT][2];   // Q^T as mma B fragments
@@ -314,6 +325,11 @@ struct ConsumerState {
                 }
             }
         }
+        if (!MULTI || GW != GP) {   // every n-tile of the warp sees its rows
+            need = kAllNeed;
+            nt_any = kAllNt;
+        }
+        if (!MULTI) col_ok = kAllCols;
     }
 
     __device__ __forceinline__ int head_of(int nt, int hc) const {
@@ -371,8 +387,6 @@ struct ConsumerState {
         const uint64_t wmask = (mask >> (kg * kRows)) & rows_mask;
         if (wmask == 0) return;               // no valid row: the state is unchanged
         const bool all_valid = wmask == rows_mask;
-        constexpr uint32_t kAllCols = (Gm::MT * Gm::NT * 4 >= 32) ? 0xffffffffu
-                                                                  : ((1u << (Gm::MT * Gm::NT * 4)) - 1u);
         const bool all_cols = col_ok == kAllCols;
 
         // S^T[row, head] = sum_d K[row, d] * Q[head, d]
@@ -762,7 +776,7 @@ __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& 
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int VAR, int D, int GP, int GW = GP>
+template <int VAR, int D, int GP, int GW = GP, bool MULTI = false>
 __global__ void __launch_bounds__(Roles<VAR>::kThreads, 1)
 decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const Params p) {
@@ -926,11 +940,16 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * 128u;
             int bt_b = -1, bt_base = -1;   // current batch: slots [bt_base, bt_base + 32) of sequence bt_b
             int bt_cur = -1, bt_nxt = -1;
-            for (int t = t0; t < t1 && ok;) {
+            // producer warp pw takes the tiles t0 + pw, t0 + pw + NPW, ...; `it` stays the tile's
+            // index in this CTA's range, which fixes its stage and phase
+            constexpr int NPW = Roles<VAR>::kProducerWarps;
+            const int pw = warp - kConsumerWarps;
+            it = pw;
+            for (int t = t0 + pw; t < t1 && ok;) {
                 const Unit U = VAR == kDense ? locate_dense(p, t, dlen, dtiles) : locate_paged(p, sm, t);
                 const int tend = min(t1, U.base + U.nt);
                 const int npages_seq = VAR == kPaged ? (U.len + P - 1) / P : 0;
-                for (; t < tend; ++t, ++it) {
+                for (; t < tend; t += NPW, it += NPW) {
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1;
                     if (!mbar_wait(sm.empty + s, ph ^ 1u, sm.abort, kWaitLimitNs)) { ok = false; break; }
@@ -1019,8 +1038,8 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 *sm.abort = 1;
                 record_error(p.err, kErrWaitEmpty);
                 if (lane == 0) {
-                    // let every load already issued land before the CTA can exit
-                    for (int k = it - S < 0 ? 0 : it - S; k < it; ++k) {
+                    // let every load this warp issued land before the CTA can exit
+                    for (int k = it - NPW; k >= 0 && k >= it - S; k -= NPW) {
                         if (!mbar_wait(sm.full + (k % S), (k / S) & 1, nullptr, kWaitLimitNs)) {
                             record_error(p.err, kErrDrain);
                             break;
@@ -1036,7 +1055,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int rb_shift = VAR == kPaged ? 31 - __clz(min(p.page_size * p.kh, kTileKeys)) : 6;
     const int kh = VAR == kPaged ? p.kh : 1;
     const int head_shift = VAR == kPaged ? 31 - __clz(p.page_size) : 6;
-    ConsumerState<D, GP, GW> cs;
+    ConsumerState<D, GP, GW, MULTI> cs;
     cs.init(warp, lane, p.G * p.sq, kh, rb_shift, head_shift, p.sq);
     uint32_t gphase = 0;
 

@@ -1,21 +1,16 @@
-// paged decode-attention kernel instantiations (head dim 64/128, padded group 8/16/32/64, and
-// the warp-per-KV-head column layout for 16-column units).
+// paged decode-attention kernel instantiations for units of one KV head (head dim 64/128, padded
+// group 8/16/32/64): every consumer mask is a compile-time constant.
 #include "launch.h"
 
 namespace da {
 
-template <int D, int GP, int GW = GP>
+template <int D, int GP>
 static cudaError_t run_paged(const Launch& L) {
-    return launch_kernel(reinterpret_cast<const void*>(&decode_attn_kernel<kPaged, D, GP, GW>),
+    return launch_kernel(reinterpret_cast<const void*>(&decode_attn_kernel<kPaged, D, GP, GP, false>),
                          Geometry<D, GP>::kSmemBytes, L);
 }
 
-cudaError_t launch_paged(int D, int GP, bool warp_head, const Launch& L) {
-    if (warp_head) {
-        if (GP != 16) return cudaErrorInvalidValue;
-        return D == 64 ? run_paged<64, 16, 8>(L) : D == 128 ? run_paged<128, 16, 8>(L)
-                                                           : cudaErrorInvalidValue;
-    }
+cudaError_t launch_paged_single(int D, int GP, const Launch& L) {
     if (D == 64) {
         switch (GP) {
             case 8: return run_paged<64, 8>(L);

@@ -23,9 +23,11 @@ int kernel_smem_bytes(int D, int GP);
 int kernel_stages(int D, int GP);
 
 cudaError_t launch_dense(int D, int GP, const Launch& L);
-// warp_head: each consumer warp holds only the query columns of the KV head its rows belong to
-// (units of kh > 1 KV heads, pages of >= 16 rows, <= 8 columns per KV head, GP == 16).
-cudaError_t launch_paged(int D, int GP, bool warp_head, const Launch& L);
+// Paged units of one KV head (kh == 1).
+cudaError_t launch_paged_single(int D, int GP, const Launch& L);
+// Paged units of kh > 1 KV heads.  warp_head: each consumer warp holds only the query columns of
+// the KV head its rows belong to (pages of >= 16 rows, <= 8 columns per KV head, GP == 16).
+cudaError_t launch_paged_multi(int D, int GP, bool warp_head, const Launch& L);
 cudaError_t launch_sparse(int D, int GP, const Launch& L);
 
 // One 32-thread block whose bounded wait on a never-completed barrier times out after limit_ns
