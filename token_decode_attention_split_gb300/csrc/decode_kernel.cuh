@@ -759,15 +759,16 @@ __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& 
         }
     }
     if (!whole) {
-        __threadfence();
+        // The group barrier orders every consumer's partial-row stores before thread 0's
+        // release on the unit's counter; the CTA that takes the counter to nseg acquires all
+        // segments' rows there, and the next group barrier hands that on to its other threads.
         if (!group_sync(sm, gphase, p.err)) return false;
         if (tid == 0) {
-            const unsigned prev = atomicAdd(p.counters + U.cu, 1u);
+            const unsigned prev = atomic_add_acq_rel_gpu(p.counters + U.cu);
             *sm.last_flag = (prev == static_cast<unsigned>(nseg - 1)) ? 1 : 0;
         }
         if (!group_sync(sm, gphase, p.err)) return false;
         if (*sm.last_flag) {
-            __threadfence();
             if (!merge_unit<D, GP>(p, sm, U, first_seg, nseg, gphase)) return false;
             if (tid == 0) p.counters[U.cu] = 0u;
         }

@@ -70,6 +70,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// ---------------------------------------------------------------- cross-CTA counters
+// Adds 1 to *ctr at GPU scope with acquire-release ordering; returns the previous value.
+__device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned* ctr) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(ctr) : "memory");
+    return old;
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Blocks until every grid this launch depends on has completed and its memory is visible (a
 // no-op when the launch has no programmatic dependency).
