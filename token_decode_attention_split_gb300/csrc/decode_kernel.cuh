@@ -77,7 +77,7 @@ struct Geometry {
     static constexpr int MT = kTileKeys / 16 / KS;              // 16-row m-tiles per warp
     static constexpr int KSTEPS = D / 16;                       // k-steps of S^T = K Q^T
     static constexpr int DT = D / 16;                           // 16-row d tiles of O^T
-    static constexpr int kMergeFloats = KS * GP * D + 2 * KS * GP;
+    static constexpr int kMergeFloats = KS * GP * D + 2 * KS * GP + 4 * GP;   // + per-head stats
     static constexpr int kMiscBytes = 1024;                     // barriers, masks, flags
     static constexpr int kSchedBytes = (2 * kMaxPagedBatch + 2) * 4;
     static constexpr int kFixedBytes = kMergeFloats * 4 + kMiscBytes + kSchedBytes;
@@ -136,6 +136,9 @@ struct SmemPtrs {
     float* merge_o;
     float* merge_m;
     float* merge_l;
+    float* head_inv;   // [GP] 1 / (sum of weights), 0 for an empty head
+    float* head_lse;   // [GP] log2-domain log-sum-exp of the head's slots
+    int* head_live;    // [GP] bit k: merge slot k holds a live piece
     uint64_t* full;
     uint64_t* empty;
     uint64_t* group;
@@ -157,6 +160,9 @@ __device__ __forceinline__ SmemPtrs carve_smem(unsigned char* raw) {
     s.merge_o = reinterpret_cast<float*>(p);
     s.merge_m = s.merge_o + Gm::KS * GP * D;
     s.merge_l = s.merge_m + Gm::KS * GP;
+    s.head_inv = s.merge_l + Gm::KS * GP;
+    s.head_lse = s.head_inv + GP;
+    s.head_live = reinterpret_cast<int*>(s.head_lse + GP);
     p += Gm::kMergeFloats * 4;
     p = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15));
     s.full = reinterpret_cast<uint64_t*>(p);
@@ -730,13 +736,16 @@ __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& 
 
     const size_t out_row0 = static_cast<size_t>(U.hq0);
     const size_t SH = static_cast<size_t>(p.seg_heads);
-    for (int idx = tid; idx < U.nh * D; idx += kConsumerThreads) {
-        const int h = idx / D, d = idx - h * D;
+    // Per head, once: the slots' weights relative to the largest slot maximum (stored over the
+    // maxima), which slots are live, 1 / (sum of weights) and the log-sum-exp.  A dead slot
+    // (maximum -inf) is skipped, and sums start from the first live term.
+    if (tid < U.nh) {
+        const int h = tid;
         float M = -CUDART_INF_F;
 #pragma unroll
         for (int k = 0; k < Gm::KS; ++k) M = fmaxf(M, sm.merge_m[k * GP + h]);
-        float L = 0.f, O = 0.f;
-        bool first = true;
+        float L = 0.f;
+        int live = 0;
         if (M != -CUDART_INF_F) {
 #pragma unroll
             for (int k = 0; k < Gm::KS; ++k) {
@@ -744,20 +753,48 @@ __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& 
                 if (mk == -CUDART_INF_F) continue;
                 const float w = fast_exp2(mk - M);
                 const float lk = w * sm.merge_l[k * GP + h];
-                const float ok = w * sm.merge_o[(k * GP + h) * D + d];
-                if (first) { L = lk; O = ok; first = false; }
-                else { L += lk; O += ok; }
+                L = live ? L + lk : lk;
+                live |= 1 << k;
+                sm.merge_m[k * GP + h] = w;
             }
         }
         const bool empty = !(L > 0.f);
-        const float val = empty ? 0.f : O * (1.0f / L);
+        sm.head_inv[h] = empty ? 0.f : 1.0f / L;
+        sm.head_lse[h] = empty ? -CUDART_INF_F : M + fast_log2(L);
+        sm.head_live[h] = empty ? 0 : live;
+    }
+    if (!group_sync(sm, gphase, p.err)) return false;
+    constexpr int D4 = D / 4;
+    for (int i = tid; i < U.nh * D4; i += kConsumerThreads) {
+        const int h = i / D4, d = (i - h * D4) * 4;
+        const int live = sm.head_live[h];
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        bool first = true;
+#pragma unroll
+        for (int k = 0; k < Gm::KS; ++k) {
+            if (!((live >> k) & 1)) continue;
+            const float w = sm.merge_m[k * GP + h];
+            const float4 o = *reinterpret_cast<const float4*>(sm.merge_o + (k * GP + h) * D + d);
+            if (first) {
+                O = make_float4(w * o.x, w * o.y, w * o.z, w * o.w);
+                first = false;
+            } else {
+                O.x += w * o.x; O.y += w * o.y; O.z += w * o.z; O.w += w * o.w;
+            }
+        }
+        const float inv = sm.head_inv[h];
+        const float4 v = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
         if (whole) {
-            p.out[(out_row0 + h) * D + d] = __float2bfloat16_rn(val);
+            __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+            uint2 packed;
+            packed.x = *reinterpret_cast<uint32_t*>(&lo);
+            packed.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(p.out + (out_row0 + h) * D + d) = packed;
         } else {
-            p.part_o[(static_cast<size_t>(seg) * SH + h) * D + d] = val;
-            if (d == 0) p.part_lse[static_cast<size_t>(seg) * SH + h] = empty ? -CUDART_INF_F : M + fast_log2(L);
+            *reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(seg) * SH + h) * D + d) = v;
         }
     }
+    if (!whole && tid < U.nh) p.part_lse[static_cast<size_t>(seg) * SH + tid] = sm.head_lse[tid];
     if (!whole) {
         // The group barrier orders every consumer's partial-row stores before thread 0's
         // release on the unit's counter; the CTA that takes the counter to nseg acquires all
