@@ -34,7 +34,8 @@ METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and µs per call"
 NOMINAL_HBM_GBS = 8000.0     # the ~8 TB/s nominal HBM3e figure of a GB300, context only
 DEFAULT_WORKLOAD = "dense_batched"
 KERNEL_SOURCES = ["token_decode_attention_split_gb300/csrc/decode_kernel.cuh",
-                  "token_decode_attention_split_gb300/csrc/ptx.cuh"]
+                  "token_decode_attention_split_gb300/csrc/ptx.cuh",
+                  "token_decode_attention_split_gb300/csrc/append.cu"]
 
 
 def kernel_sha() -> str:
@@ -514,7 +515,9 @@ def run_native(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": f"decode_attn_kernel<{c0.kind}>", "timing": "cuda graph of K calls",
+                     "kernel": ("append_kernel" if c0.kind == "append"
+                                else f"decode_attn_kernel<{c0.kind}>"),
+                     "timing": "cuda graph of K calls",
                      "launch_us": round(launch_ms * 1e3, 2)},
         "clocks": clk,
         "wall_s_timed_region": round(wall, 4),

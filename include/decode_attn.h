@@ -152,7 +152,7 @@ da_status decode_attn_paged_mq(const void *q, const void *k_pool, const void *v_
  * pads up to the fixed width); each valid entry adds its row once (duplicates count once per
  * entry); a -1 entry adds an exact zero to the denominator and nothing to the output.
  * Appending -1 pads to a selection leaves every output bit unchanged: the work is split into
- * chunks of 512 * ceil(G / 16) entries (G = Hq / Hkv) that depend on nothing else, not on the
+ * chunks of 512 * ceil(G / 32) entries (G = Hq / Hkv) that depend on nothing else, not on the
  * width, B or the device.
  *   1 <= pool_rows < 2^31; width >= 0 (width = 0 writes zeros).
  */

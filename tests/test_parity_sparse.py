@@ -21,8 +21,8 @@ CASES = [
     (2, 64, 8, 128, 1500, 1000, 64, 300),   # G = 8
     (2, 16, 1, 128, 900, 256, 8, 0),        # G = 16, exactly one chunk
     (2, 32, 1, 64, 800, 513, 8, 100),       # G = 32
-    (1, 48, 1, 128, 5000, 2048, 128, 512),  # G = 48: three head groups, two chunks
-    (2, 64, 1, 128, 9000, 5000, 128, 300),  # G = 64: four head groups, three chunks
+    (1, 48, 1, 128, 5000, 2048, 128, 512),  # G = 48: head groups of 32 and 16, two chunks
+    (2, 64, 1, 128, 9000, 5000, 128, 300),  # G = 64: two head groups, five chunks
     (2, 16, 2, 64, 3000, 1100, 32, 50),     # G = 16: three chunks
 ]
 

@@ -174,11 +174,11 @@ int persistent_ctas(int dev) {
     return (lim > 0 && lim < sms) ? lim : sms;
 }
 
-// Sparse work split: query-head groups of 16 when G > 16, and chunks of 512 selection entries
+// Sparse work split: query-head groups of 32 when G > 32, and chunks of 512 selection entries
 // per head group.  Both depend on G only, never on the width, B or the device.
 int sparse_head_groups(int G) { return G <= kSparseHeadGroup ? 1 : (G + kSparseHeadGroup - 1) / kSparseHeadGroup; }
 int sparse_segment_heads(int G) { return G <= kSparseHeadGroup ? G : kSparseHeadGroup; }
-int sparse_padded_group(int G) { return G <= 8 ? 8 : 16; }
+int sparse_padded_group(int G) { return G <= 8 ? 8 : G <= 16 ? 16 : 32; }
 long long sparse_chunk_keys(int G) { return static_cast<long long>(kSparseChunkUnit) * sparse_head_groups(G); }
 long long sparse_chunks(long long width, int G) { return (width + sparse_chunk_keys(G) - 1) / sparse_chunk_keys(G); }
 

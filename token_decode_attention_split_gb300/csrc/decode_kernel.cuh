@@ -55,7 +55,7 @@ struct Roles {
     static constexpr int kThreads = kConsumerThreads + 32 * kProducerWarps;
 };
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr int kSparseHeadGroup = 16;         // query heads per CTA when a group is split
+constexpr int kSparseHeadGroup = 32;         // query heads per CTA when a group is split
 constexpr int kSparseChunkUnit = 512;         // sparse chunk = 512 entries per head group
 constexpr int kMaxPagedBatch = 1024;
 constexpr int kSmemBudget = 232448;           // opt-in dynamic shared memory per block

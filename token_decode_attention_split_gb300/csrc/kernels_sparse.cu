@@ -1,5 +1,5 @@
-// sparse decode-attention kernel instantiations (head dim 64/128; a CTA takes at most 16
-// query heads, so only the padded groups 8 and 16 exist).
+// sparse decode-attention kernel instantiations (head dim 64/128; a CTA takes at most 32
+// query heads, so only the padded groups 8, 16 and 32 exist).
 #include "launch.h"
 
 namespace da {
@@ -15,11 +15,13 @@ cudaError_t launch_sparse(int D, int GP, const Launch& L) {
         switch (GP) {
             case 8: return run_sparse<64, 8>(L);
             case 16: return run_sparse<64, 16>(L);
+            case 32: return run_sparse<64, 32>(L);
         }
     } else if (D == 128) {
         switch (GP) {
             case 8: return run_sparse<128, 8>(L);
             case 16: return run_sparse<128, 16>(L);
+            case 32: return run_sparse<128, 32>(L);
         }
     }
     return cudaErrorInvalidValue;
