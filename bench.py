@@ -33,14 +33,18 @@ from token_decode_attention_split_gb300 import workloads as W  # noqa: E402
 METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and µs per call"
 NOMINAL_HBM_GBS = 8000.0     # the ~8 TB/s nominal HBM3e figure of a GB300, context only
 DEFAULT_WORKLOAD = "dense_batched"
-KERNEL_SOURCES = ["token_decode_attention_split_gb300/csrc/decode_kernel.cuh",
-                  "token_decode_attention_split_gb300/csrc/ptx.cuh",
-                  "token_decode_attention_split_gb300/csrc/append.cu"]
+KERNEL_SOURCES = {
+    "decode": ["token_decode_attention_split_gb300/csrc/decode_kernel.cuh",
+               "token_decode_attention_split_gb300/csrc/ptx.cuh"],
+    "append": ["token_decode_attention_split_gb300/csrc/append.cu",
+               "token_decode_attention_split_gb300/csrc/ptx.cuh"],
+}
 
 
-def kernel_sha() -> str:
+def kernel_sha(kind: str = "decode") -> str:
+    """First 16 hex digits of the sha256 of the sources of the kernel a workload times."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES["append" if kind == "append" else "decode"]:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -64,7 +68,7 @@ def traffic_record(workload: str):
         with open(path) as f:
             d = json.load(f)
         rec = d.get(workload)
-        if rec and rec.get("kernel_sha") == kernel_sha():
+        if rec and rec.get("kernel_sha") == kernel_sha(W.CONFIGS[workload]["kind"]):
             return float(rec["bytes_per_launch"])
     except Exception:
         pass
