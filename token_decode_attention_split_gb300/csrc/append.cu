@@ -4,8 +4,10 @@
 //                             the paged-cache slot slot_mapping[t] (i64) of every KV head.
 //   decode_attn_append_ring   "AttnV41" (attn_v41), method decode_body: the window ring write at
 //                             pos % window, the position read on the device.
-// Both are plain HBM-bound copies: one warp moves one (row, KV head) of K and of V with 16-byte
-// loads and stores; the slot or position is read on the device and never validated by a sync.
+// Both are plain HBM-bound copies: one warp moves one new row (K and V of every KV head) with
+// 16-byte loads issued in batches before their stores, so a warp waits on memory about twice per
+// row (its slot word, then the row's data); the slot or position is read on the device and never
+// validated by a sync.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -15,7 +17,8 @@
 
 namespace {
 
-constexpr int kAppendThreads = 256;   // 8 warps, one (row, KV head) each per step
+constexpr int kAppendThreads = 256;   // 8 warps, one new row each per step
+constexpr int kAppendBatch = 8;       // 16-byte loads in flight per lane
 
 struct AppendArgs {
     const uint4* k_new;   // [rows, Hkv, D] as 16-byte chunks
@@ -33,16 +36,22 @@ struct AppendArgs {
     int ring;
 };
 
-// Destination row (in units of rows of D elements) of (row, KV head g), or -1 to skip.
-__device__ __forceinline__ int64_t dest_row(const AppendArgs& a, int64_t row, int g) {
+// First destination row (in rows of D elements) of new row `row` and the stride between its KV
+// heads' destination rows, or false when the slot or position says to skip the row.
+__device__ __forceinline__ bool dest_rows(const AppendArgs& a, int64_t row, int64_t& base,
+                                          int64_t& head_stride) {
     const int64_t w = a.where[row];
     if (a.ring) {
-        if (w < 0) return -1;
-        return (row * a.Hkv + g) * a.pool_rows + w % a.window;
+        if (w < 0) return false;
+        base = row * a.Hkv * a.pool_rows + w % a.window;
+        head_stride = a.pool_rows;
+        return true;
     }
-    if (w < 0 || w >= a.num_slots) return -1;
+    if (w < 0 || w >= a.num_slots) return false;
     const int64_t page = w / a.page_size, off = w - page * a.page_size;
-    return (page * a.Hkv + g) * a.page_size + off;
+    base = page * a.Hkv * a.page_size + off;
+    head_stride = a.page_size;
+    return true;
 }
 
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs a) {
@@ -50,20 +59,32 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
     da::allow_dependent_launch();
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (kAppendThreads / 32);
-    const int64_t total = a.rows * a.Hkv;
-    for (int64_t wi = blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5); wi < total;
-         wi += warps) {
-        const int64_t row = wi / a.Hkv;
-        const int g = static_cast<int>(wi - row * a.Hkv);
-        const int64_t dst = dest_row(a, row, g);
-        if (dst < 0) continue;
-        const int64_t src = (row * a.Hkv + g) * a.chunks;
-        const int64_t dc = dst * a.chunks;
-        for (int c = lane; c < 2 * a.chunks; c += 32) {
-            const bool isv = c >= a.chunks;
-            const int cc = isv ? c - a.chunks : c;
-            const uint4 x = __ldg((isv ? a.v_new : a.k_new) + src + cc);
-            (isv ? a.v_pool : a.k_pool)[dc + cc] = x;
+    const int half = a.Hkv * a.chunks;    // 16-byte chunks of one new row's K (or V), all heads
+    for (int64_t row = blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5); row < a.rows;
+         row += warps) {
+        int64_t base, head_stride;
+        if (!dest_rows(a, row, base, head_stride)) continue;
+        const int64_t src0 = row * half;
+        for (int c0 = 0; c0 < 2 * half; c0 += 32 * kAppendBatch) {
+            uint4 x[kAppendBatch];
+#pragma unroll
+            for (int i = 0; i < kAppendBatch; ++i) {
+                const int c = c0 + i * 32 + lane;
+                if (c < 2 * half) {
+                    const bool isv = c >= half;
+                    x[i] = __ldg((isv ? a.v_new : a.k_new) + src0 + (isv ? c - half : c));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kAppendBatch; ++i) {
+                const int c = c0 + i * 32 + lane;
+                if (c < 2 * half) {
+                    const bool isv = c >= half;
+                    const int r = isv ? c - half : c;          // chunk within K (or V) of all heads
+                    const int g = r / a.chunks, cc = r - g * a.chunks;
+                    (isv ? a.v_pool : a.k_pool)[(base + g * head_stride) * a.chunks + cc] = x[i];
+                }
+            }
         }
     }
 }
@@ -71,7 +92,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 da_status launch(const AppendArgs& a, void* stream) {
-    const int64_t work = a.rows * a.Hkv;
+    const int64_t work = a.rows;
     if (work == 0) return DA_OK;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
