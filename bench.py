@@ -361,6 +361,13 @@ def cpu_baseline(name: str, budget_s: float = 15.0):
                       f"workload's algorithmic bytes / time"}
 
 
+def workload_config(name: str, **extra):
+    """The line's `config`: the workload's name and fields (with any overrides) plus `extra`."""
+    return {"workload": name + ("" if not OVERRIDES else " (overridden)"),
+            **{k: v for k, v in {**W.CONFIGS[name], **OVERRIDES}.items() if k != "seed"},
+            **extra}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -379,7 +386,8 @@ def run_reference(args, world, rank):
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(total * per_byte * 1e3, 4), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16 copy", "data": "synthetic",
-                "config": {"workload": name},
+                "config": workload_config(name, algorithmic_bytes_per_call=int(total),
+                                          l2="n/a (CPU)", parallelism="oracle on one host core"),
                 "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1,
                                  "kind": "oracle", "sample": f"{rows} rows per step"},
                 "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -387,7 +395,7 @@ def run_reference(args, world, rank):
         print(json.dumps(line), flush=True)
         return
     c = cpu_case(name)
-    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    per_step = max(0.2, 4.0 * args.cpu_budget / max(1, args.steps + args.warmup))
     times = []
     rows_used = 0
     threads = os.cpu_count() or 1
@@ -404,7 +412,8 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs_full * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": name, "l2": "n/a (CPU)"},
+        "config": workload_config(name, algorithmic_bytes_per_call=int(c.algorithmic_bytes()),
+                                  l2="n/a (CPU)", parallelism="oracle on the host cores"),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle",
                          "sample": f"{rows_used} of {c.B * c.Hq} (b, h) rows per step, scaled "
@@ -506,12 +515,10 @@ def run_native(args, world, rank, local):
         "pct_of_nominal_8tbs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": name + ("" if not OVERRIDES else " (overridden)"),
-                   **{k: v for k, v in {**W.CONFIGS[name], **OVERRIDES}.items() if k != "seed"},
-                   "algorithmic_bytes_per_call": int(bytes_step),
-                   "algorithmic_bytes_per_copy": [int(a) for a in alg],
-                   "l2": "inputs larger than L2; two input copies alternated",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(name, algorithmic_bytes_per_call=int(bytes_step),
+                                  algorithmic_bytes_per_copy=[int(a) for a in alg],
+                                  l2="inputs larger than L2; two input copies alternated",
+                                  parallelism=f"replicas x{world}"),
         "e2e": {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_ms, 4)},

@@ -1,0 +1,41 @@
+"""The benchmark's reference arm on the CPU: `bench.py --impl reference` times the fp64 oracle and
+prints one JSON line with the fields the native arm prints (metric, unit, config of the same
+workload, e2e and cpu_baseline describing the run)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_reference(workload):
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", workload,
+                          "--steps", "3", "--warmup", "3", "--cpu-budget", "0.5"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    return json.loads(lines[0])
+
+
+@pytest.mark.parametrize("workload", ["dense_tiny", "append_paged"])
+def test_reference_line(workload):
+    import bench
+    from token_decode_attention_split_gb300 import workloads as W
+    d = run_reference(workload)
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3
+    assert d["value"] > 0 and d["e2e"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    cfg = d["config"]
+    assert cfg["workload"] == workload
+    for k, v in W.CONFIGS[workload].items():
+        if k != "seed":
+            assert cfg[k] == v
+    assert cfg["algorithmic_bytes_per_call"] > 0
