@@ -41,12 +41,37 @@ KERNEL_SOURCES = {
 }
 
 
+def code_only(src: str) -> str:
+    """C/C++ source without comments, whitespace runs collapsed (string literals kept)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            i = src.find("*/", i + 2)
+            i = n if i < 0 else i + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_sha(kind: str = "decode") -> str:
-    """First 16 hex digits of the sha256 of the sources of the kernel a workload times."""
+    """First 16 hex digits of the sha256 of the code (comments and layout aside) of the sources
+    of the kernel a workload times."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES["append" if kind == "append" else "decode"]:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

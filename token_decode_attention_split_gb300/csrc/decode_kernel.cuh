@@ -1,28 +1,31 @@
 // Single-query decode attention on sm_103a: one kernel per call.
 //
-// Work decomposition.  A "unit" is one (sequence b, KV head g); its G = Hq/Hkv query heads are
-// processed together so every K/V row is read from HBM exactly once.  Paged units may take kh
-// adjacent KV heads (kh * G query heads): a page of kh adjacent heads is kh * page_size
-// contiguous rows, so with kh * page_size = 64 a paged tile is one 64-row TMA box per half, the
-// same transfer as a dense tile; each query-head column then only sees its own KV head's rows.  A unit's live rows are cut
-// into 64-row tiles.  Dense and paged calls run a persistent grid (one CTA per SM): the tiles of
-// all units are laid end to end and CTA c takes the contiguous range [c*N/C, (c+1)*N/C), so the
-// load is balanced to one tile whatever the lengths.  Sparse calls give each CTA up to 16 query
-// heads of one unit over one chunk of 512 * ceil(G / 16) selection entries: the chunk depends on
-// G only, so trailing -1 pads cannot move a chunk boundary, and the usual top-k width of a few
-// thousand entries needs no merge.  Each CTA's piece of a unit is a "segment".
+// Work decomposition.  A "unit" is one (sequence b, KV head g); its G = Hq/Hkv query heads (times
+// the query tokens, for several tokens per sequence) are processed together so every K/V row is
+// read from HBM exactly once.  Paged units may take kh adjacent KV heads (kh * G query columns):
+// a page of kh adjacent heads is kh * page_size contiguous rows, so with kh * page_size = 64 a
+// paged tile is one 64-row TMA box per half, the same transfer as a dense tile; each query
+// column then only sees its own KV head's rows.  A unit's live rows are cut into 64-row tiles.
+// Dense and paged calls run a persistent grid (one CTA per SM): the tiles of all units are laid
+// end to end and CTA c takes the contiguous range [c*N/C, (c+1)*N/C), so the load is balanced to
+// one tile whatever the lengths.  Sparse calls give each CTA up to 32 query heads of one unit
+// over one chunk of 512 * ceil(G / 32) selection entries: the chunk depends on G only, so
+// trailing -1 pads cannot move a chunk boundary.  Each CTA's piece of a unit is a "segment".
 //
-// Inside a CTA.  Warp 4 is the producer: it streams K and V tiles into a ring of shared-memory
-// stages (TMA tile loads with 128-byte swizzle for dense and paged; cp.async 16-byte gathers with
-// the same swizzle for sparse) and posts a per-stage validity mask.  Warps 0-3 consume: the GQA
-// group sits on the N side of mma.m16n8k16 (S^T = K * Q^T, then O^T += V^T * P^T), so each
-// K/V element read from shared memory feeds all G heads; the online softmax (running max, sum and
-// accumulator) stays in fp32 registers.
+// Inside a CTA.  The producer warps (one for dense, two taking alternate tiles for paged, four
+// sharing every tile for sparse) stream K and V tiles into a ring of shared-memory stages (TMA
+// tile loads with 128-byte swizzle for dense and paged; cp.async 16-byte gathers with the same
+// swizzle for sparse) and post a per-stage validity mask.  Warps 0-3 consume: the GQA group
+// sits on the N side of mma.m16n8k16 (S^T = K * Q^T, then O^T += V^T * P^T), so each K/V
+// element read from shared memory feeds all G heads; the online softmax (running max, sum and
+// accumulator) stays in fp32 registers.  For units of one KV head every column mask is a
+// compile-time constant, so a stage's MMAs are straight-line code.
 //
 // Merge.  A segment covering a whole unit writes the bf16 output directly.  Otherwise it writes
-// its normalised partial row and log2-sum-exp to the workspace and bumps the unit's counter; the
-// CTA that completes the unit merges all its partials by log-sum-exp in segment order (so the
-// result does not depend on which CTA finishes last) and resets the counter to zero.
+// its normalised partial row and log2-sum-exp to the workspace and bumps the unit's counter
+// (acquire-release); the CTA that completes the unit merges all its partials by log-sum-exp in
+// segment order (so the result does not depend on which CTA finishes last) and resets the
+// counter to zero.
 //
 // Launch.  Kernels are launched with programmatic stream serialization: a CTA sets up its shared
 // memory while the previous kernel in the stream drains, then waits for that kernel's completion
