@@ -29,8 +29,11 @@ CASES = [
     (2, 64, 8, 128, 128, 64, 100, 900, 1),
     (2, 16, 16, 128, 256, 32, 200, 1000, 3),
     (3, 64, 1, 128, 16, 300, 1, 800, 1),
-    (3, 32, 8, 128, 8, 2048, 1, 700, 1),    # 8-row pages: four KV heads per unit
+    (3, 32, 8, 128, 8, 2048, 1, 700, 1),    # 8-row pages: eight KV heads (32 columns) per unit
     (2, 24, 8, 64, 16, 600, 5, 900, 3),     # G = 3, D = 64: four KV heads per unit
+    (2, 64, 8, 128, 8, 1024, 1, 500, 1),    # G = 8, 8-row pages: eight KV heads, 64 columns
+    (2, 32, 2, 128, 64, 200, 1, 700, 1),    # G = 16: one KV head (16 columns) per unit
+    (2, 64, 2, 64, 128, 100, 1, 800, 3),    # G = 32, D = 64: one KV head (32 columns) per unit
 ]
 
 
