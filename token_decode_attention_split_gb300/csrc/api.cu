@@ -167,6 +167,9 @@ int paged_kv_heads(int Hkv, int G, int page_size) {
     return kh;
 }
 
+// Dense units of at most this many 64-row tiles are not split across CTAs.
+constexpr long long kShortUnitTiles = 8;
+
 // CTAs for a persistent dense/paged launch on `dev`.
 int persistent_ctas(int dev) {
     const int sms = sm_count(dev);
@@ -392,8 +395,11 @@ da_status run_dense(const void* q, const void* k, const void* v, void* out, int 
     L.p.sq = sq;
     L.p.causal = causal ? 1 : 0;
     L.p.seg_heads = G * sq;
+    // Short units (a few tiles) go whole to one CTA each: splitting them would trade a few
+    // tiles of streaming for a cross-CTA merge that costs more.
+    const long long spread = tiles <= kShortUnitTiles ? units : units * tiles;
     L.grid = static_cast<int>(k_len_dev ? persistent_ctas(dev)
-                                        : std::min<long long>(persistent_ctas(dev), units * tiles));
+                                        : std::min<long long>(persistent_ctas(dev), spread));
     L.stream = cs;
     L.threads = Roles<kDense>::kThreads;
     return launch_dense(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
