@@ -395,9 +395,12 @@ da_status run_dense(const void* q, const void* k, const void* v, void* out, int 
     L.p.sq = sq;
     L.p.causal = causal ? 1 : 0;
     L.p.seg_heads = G * sq;
-    // Short units (a few tiles) go whole to one CTA each: splitting them would trade a few
-    // tiles of streaming for a cross-CTA merge that costs more.
-    const long long spread = tiles <= kShortUnitTiles ? units : units * tiles;
+    // Whole units, one per CTA, when they are short (splitting would trade a few tiles of
+    // streaming for a cross-CTA merge that costs more) or when they are about as many as the SMs
+    // (equal-length units then stream without any split, on at least 80% of the SMs);
+    // otherwise every tile is spread over all SMs.
+    const bool whole_units = tiles <= kShortUnitTiles || (5 * units >= 4LL * sms && units <= sms);
+    const long long spread = whole_units ? units : units * tiles;
     L.grid = static_cast<int>(k_len_dev ? persistent_ctas(dev)
                                         : std::min<long long>(persistent_ctas(dev), spread));
     L.stream = cs;
