@@ -308,33 +308,42 @@ def oracle_sample_run(case_host, budget_s: float):
     # size the sample from a short probe
     probe = np.arange(min(n, max(1, threads)), dtype=np.int64)
     t0 = time.perf_counter()
-    _run_oracle(case_host, probe, threads)
+    done = _run_oracle(case_host, probe, threads)
     dt = max(time.perf_counter() - t0, 1e-6)
-    per_row = dt / len(probe)
+    per_row = dt / done
     rows = int(max(1, min(n, budget_s / per_row)))
     pairs = np.linspace(0, n - 1, rows).round().astype(np.int64)
     pairs = np.unique(pairs)
     # a sample shorter than the budget is repeated (whole passes) to fill about half of it
-    passes, t0 = 0, time.perf_counter()
+    passes, done, t0 = 0, 0, time.perf_counter()
     while True:
-        _run_oracle(case_host, pairs, threads)
+        done += _run_oracle(case_host, pairs, threads)
         passes += 1
         el = time.perf_counter() - t0
         if el >= budget_s / 2 or passes >= 1000:
             break
-    return len(pairs) * passes, el, threads
+    return done, el, threads
 
 
 def _run_oracle(c, pairs, threads):
+    """The oracle on the (b, h) rows `pairs` of a host case; returns the rows it computed (for
+    several query tokens, every head of each sequence that `pairs` touches)."""
     import oracle
+    if c.kind == "dense" and c.sq > 1:
+        bs = np.unique(np.asarray(pairs) // c.Hq)
+        oracle.dense_mq(c.q[bs], c.k[bs], c.v[bs], c.k_len, c.scale, causal=bool(c.causal),
+                        nthreads=threads)
+        return len(bs) * c.Hq
     if c.kind == "dense":
-        return oracle.dense(c.q, c.k, c.v, c.k_len, c.scale, pairs=pairs, nthreads=threads)
-    if c.kind == "paged":
-        return oracle.paged(c.q, c.k_pool, c.v_pool, c.block_table.numpy(),
-                            c.kv_args.numpy().view(np.uint32), c.scale,
-                            kv_len_stride=c.kv_len_stride, pairs=pairs, nthreads=threads)
-    return oracle.sparse(c.q, c.k_pool, c.v_pool, c.sel.numpy(), c.scale, pairs=pairs,
-                         nthreads=threads)
+        oracle.dense(c.q, c.k, c.v, c.k_len, c.scale, pairs=pairs, nthreads=threads)
+    elif c.kind == "paged":
+        oracle.paged(c.q, c.k_pool, c.v_pool, c.block_table.numpy(),
+                     c.kv_args.numpy().view(np.uint32), c.scale,
+                     kv_len_stride=c.kv_len_stride, pairs=pairs, nthreads=threads)
+    else:
+        oracle.sparse(c.q, c.k_pool, c.v_pool, c.sel.numpy(), c.scale, pairs=pairs,
+                      nthreads=threads)
+    return len(pairs)
 
 
 def cpu_case(name):
@@ -463,7 +472,7 @@ def run_native(args, world, rank, local):
     else:
         var = {"dense": 0, "paged": 1, "sparse": 2}[c0.kind]
         ws = B_.new_workspace(B_.decode_attn_workspace_size(
-            var, c0.B, c0.Hq, c0.Hkv, c0.D, getattr(c0, "width", 0)), dev)
+            var, c0.B, c0.Hq * getattr(c0, "sq", 1), c0.Hkv, c0.D, getattr(c0, "width", 0)), dev)
         outs = [torch.empty(c.out_shape(), dtype=torch.bfloat16, device=dev) for c in cases]
     stream = torch.cuda.Stream(dev)
     alg = [c.algorithmic_bytes() for c in cases]

@@ -21,7 +21,7 @@ def run_reference(workload):
     return json.loads(lines[0])
 
 
-@pytest.mark.parametrize("workload", ["dense_tiny", "append_paged"])
+@pytest.mark.parametrize("workload", ["dense_tiny", "append_paged", "dense_verify4"])
 def test_reference_line(workload):
     import bench
     from token_decode_attention_split_gb300 import workloads as W

@@ -160,3 +160,16 @@ def test_device_len_graph_replay_follows_the_length_word():
         torch.cuda.synchronize()
         ref_case = W.DenseCase(c.q, c.k, c.v, n, c.scale, c.B, c.Hq, c.Hkv, c.D, 2048)
         assert_close(out_f64(out), oracle_for(ref_case), f"replay with k_len {n}")
+
+
+def test_named_device_len_workload():
+    """dense_device_len at full size: the length word on the device, sampled rows vs the oracle."""
+    c = W.make("dense_device_len", device=DEV)
+    out = B_.run_case(c)
+    torch.cuda.synchronize()
+    n = c.B * c.Hq
+    pairs = np.unique(np.concatenate([[0, n - 1], np.random.default_rng(1).choice(n, 24, replace=False)]))
+    host = W.DenseCase(c.q.cpu(), c.k.cpu(), c.v.cpu(), c.k_len, c.scale, c.B, c.Hq, c.Hkv, c.D,
+                       c.capacity)
+    assert_close(out_f64(out).reshape(n, -1)[pairs], oracle_for(host, pairs=pairs).reshape(n, -1)[pairs],
+                 "dense_device_len")

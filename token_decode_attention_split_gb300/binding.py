@@ -239,9 +239,16 @@ def run_case(case, out=None, workspace=None, stream=None):
     if out is None:
         out = torch.empty(case.out_shape(), dtype=torch.bfloat16, device=dev)
     if case.kind == "dense":
+        sq = getattr(case, "sq", 1)
         if workspace is None:
             workspace = new_workspace(decode_attn_workspace_size(
-                DA_VARIANT_DENSE, case.B, case.Hq, case.Hkv, case.D), dev)
+                DA_VARIANT_DENSE, case.B, case.Hq * sq, case.Hkv, case.D), dev)
+        if sq > 1:
+            return decode_attn_dense_mq(case.q, case.k, case.v, out, case.k_len, case.causal,
+                                        case.scale, workspace, stream)
+        if getattr(case, "k_len_dev", None) is not None:
+            return decode_attn_dense_device_len(case.q, case.k, case.v, out, case.k_len_dev,
+                                                case.scale, workspace, stream)
         return decode_attn_dense(case.q, case.k, case.v, out, case.k_len, case.scale, workspace,
                                  stream)
     if case.kind == "paged":

@@ -395,14 +395,15 @@ da_status run_dense(const void* q, const void* k, const void* v, void* out, int 
     L.p.sq = sq;
     L.p.causal = causal ? 1 : 0;
     L.p.seg_heads = G * sq;
-    // Whole units, one per CTA, when they are short (splitting would trade a few tiles of
-    // streaming for a cross-CTA merge that costs more) or when they are about as many as the SMs
-    // (equal-length units then stream without any split, on at least 80% of the SMs);
-    // otherwise every tile is spread over all SMs.
-    const bool whole_units = tiles <= kShortUnitTiles || (5 * units >= 4LL * sms && units <= sms);
+    // Whole units, one per CTA, when they are about as many as the SMs (the units of a dense
+    // call have equal lengths, so they then stream without any split, on at least 80% of the
+    // SMs, whatever the length), or when the host knows they are short (splitting would trade a
+    // few tiles of streaming for a cross-CTA merge that costs more); otherwise every tile is
+    // spread over all SMs.
+    const bool near_sms = 5 * units >= 4LL * sms && units <= sms;
+    const bool whole_units = near_sms || (!k_len_dev && tiles <= kShortUnitTiles);
     const long long spread = whole_units ? units : units * tiles;
-    L.grid = static_cast<int>(k_len_dev ? persistent_ctas(dev)
-                                        : std::min<long long>(persistent_ctas(dev), spread));
+    L.grid = static_cast<int>(std::min<long long>(persistent_ctas(dev), spread));
     L.stream = cs;
     L.threads = Roles<kDense>::kThreads;
     return launch_dense(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;

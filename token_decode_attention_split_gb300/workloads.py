@@ -36,6 +36,12 @@ CONFIGS = {
                           poison_tail=True, seed=1002),
     "dense_long": dict(kind="dense", B=4, Hq=64, Hkv=8, D=128, capacity=131072, k_len=131071,
                        k_scale=2.0, seed=1003),
+    # the batched dense step with its length read on the device (a captured graph replays it
+    # for every token), and a 4-token verify step with causal masking inside the new tail
+    "dense_device_len": dict(kind="dense", B=16, Hq=32, Hkv=8, D=128, capacity=8192, k_len=4096,
+                             poison_tail=True, device_len=True, seed=1007),
+    "dense_verify4": dict(kind="dense", B=16, Hq=32, Hkv=8, D=128, capacity=8192, k_len=4096,
+                          poison_tail=True, sq=4, causal=1, seed=1008),
     # paged, per-sequence lengths in a device args buffer
     "paged_ragged": dict(kind="paged", B=64, Hq=32, Hkv=8, D=128, page_size=16, num_pages=160000,
                          kv_min=128, kv_max=32768, seed=1004),
@@ -89,14 +95,17 @@ class DenseCase:
     D: int
     capacity: int
     kind: str = "dense"
+    sq: int = 1                            # query tokens per sequence (q, out [B, Hq, sq, D])
+    causal: int = 0                        # sq > 1: token i attends rows [0, k_len - sq + i]
+    k_len_dev: torch.Tensor | None = None  # set: the length is read from this device word
 
     def algorithmic_bytes(self) -> int:
-        """Live K/V rows + q + out (bf16)."""
+        """Live K/V rows + q + out (bf16), + the length word when it is read on the device."""
         kv = 2 * self.B * self.Hkv * self.k_len * self.D * 2
-        return kv + 2 * self.B * self.Hq * self.D * 2
+        return kv + 2 * self.B * self.Hq * self.sq * self.D * 2 + (4 if self.k_len_dev is not None else 0)
 
     def out_shape(self):
-        return (self.B, self.Hq, 1, self.D)
+        return (self.B, self.Hq, self.sq, self.D)
 
 
 @dataclass
@@ -204,16 +213,19 @@ def make_append(T, Hkv, D, page_size, num_pages, seed, device="cpu", pad_every=0
 
 
 def make_dense(B, Hq, Hkv, D, capacity, k_len, seed, device="cpu", k_scale=1.0,
-               poison_tail=False, scale=None) -> DenseCase:
+               poison_tail=False, scale=None, sq=1, causal=0, device_len=False) -> DenseCase:
+    """sq > 1: several query tokens per sequence (q [B, Hq, sq, D]); device_len: the length is
+    also stored as one u32 word in device memory, for the call that reads it there."""
     dev, g, _ = _gens(seed, device)
-    q = _normal_bf16((B, Hq, 1, D), g, dev)
+    q = _normal_bf16((B, Hq, sq, D), g, dev)
     k = _normal_bf16((B, Hkv, capacity, D), g, dev, mult=k_scale)
     v = _normal_bf16((B, Hkv, capacity, D), g, dev)
     if poison_tail and k_len < capacity:
         k[:, :, k_len:, :] = float("nan")
         v[:, :, k_len:, :] = float("nan")
+    word = torch.tensor([int(k_len)], dtype=torch.int32, device=dev) if device_len else None
     return DenseCase(q, k, v, int(k_len), scale if scale is not None else 1.0 / math.sqrt(D),
-                     B, Hq, Hkv, D, capacity)
+                     B, Hq, Hkv, D, capacity, sq=int(sq), causal=int(causal), k_len_dev=word)
 
 
 def make_paged(B, Hq, Hkv, D, page_size, num_pages, kv_min, kv_max, seed, device="cpu",
