@@ -187,24 +187,6 @@ long long sparse_chunks(long long width, int G) { return (width + sparse_chunk_k
 
 }  // namespace
 
-int kernel_smem_bytes(int D, int GP) {
-#define DA_SMEM_CASE(d, g) \
-    if (D == d && GP == g) return Geometry<d, g>::kSmemBytes;
-    DA_SMEM_CASE(64, 8) DA_SMEM_CASE(64, 16) DA_SMEM_CASE(64, 32) DA_SMEM_CASE(64, 64)
-    DA_SMEM_CASE(128, 8) DA_SMEM_CASE(128, 16) DA_SMEM_CASE(128, 32) DA_SMEM_CASE(128, 64)
-#undef DA_SMEM_CASE
-    return 0;
-}
-
-int kernel_stages(int D, int GP) {
-#define DA_ST_CASE(d, g) \
-    if (D == d && GP == g) return Geometry<d, g>::kStages;
-    DA_ST_CASE(64, 8) DA_ST_CASE(64, 16) DA_ST_CASE(64, 32) DA_ST_CASE(64, 64)
-    DA_ST_CASE(128, 8) DA_ST_CASE(128, 16) DA_ST_CASE(128, 32) DA_ST_CASE(128, 64)
-#undef DA_ST_CASE
-    return 0;
-}
-
 cudaError_t launch_kernel(const void* kernel, int smem, const Launch& L) {
     const int dev = current_device();
     if (dev < 0) return cudaErrorInvalidDevice;

@@ -198,13 +198,6 @@ __device__ __forceinline__ uint32_t tile_offset(int r, int c, int rb_shift) {
 }
 
 // ------------------------------------------------------------------ schedule
-template <int VAR>
-struct Schedule {
-    int N;     // tiles in the whole call
-    int C;     // CTAs sharing them
-    int t0, t1;
-};
-
 __device__ __forceinline__ int tile_owner(int t, int N, int C) {
     // the CTA whose range [c*N/C, (c+1)*N/C) holds tile t
     return static_cast<int>((static_cast<long long>(t + 1) * C + N - 1) / N) - 1;

@@ -18,10 +18,6 @@ struct Launch {
     cudaStream_t stream;
 };
 
-// Dynamic shared memory bytes of the kernel for head dim D and padded group GP (0 if none).
-int kernel_smem_bytes(int D, int GP);
-int kernel_stages(int D, int GP);
-
 cudaError_t launch_dense(int D, int GP, const Launch& L);
 // Paged units of one KV head (kh == 1).
 cudaError_t launch_paged_single(int D, int GP, const Launch& L);
