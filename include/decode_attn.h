@@ -43,7 +43,9 @@
  *   - Workspace: caller-owned device scratch of at least decode_attn_workspace_size() bytes.
  *     It must be zero-filled once before its first use (decode_attn_workspace_init or
  *     cudaMemset); every completed call leaves its counters at zero again, so later calls need
- *     no clearing.  One workspace must not be shared by calls that can run concurrently.
+ *     no clearing.  One workspace must not be shared by calls that can run concurrently.  A call
+ *     that stopped on a timed-out wait (decode_attn_read_device_error returns nonzero) may leave
+ *     counters set: zero-fill the workspace again before reusing it.
  */
 #ifndef DECODE_ATTN_H
 #define DECODE_ATTN_H
