@@ -193,3 +193,19 @@ def test_multitoken_rejects(lib):
         ctypes.c_float(0.1), FAKE, ctypes.c_size_t(1 << 20), None)
     assert call(8, 2, 0) == INVALID          # no query token
     assert call(64, 2, 3) == UNSUPPORTED     # 32 heads x 3 tokens > 64 columns per unit
+
+
+def test_binding_has_every_declared_call():
+    """The Python binding exposes each C entry point under the same name."""
+    for name in declared_functions():
+        assert hasattr(binding, name), name
+
+
+def test_binding_spec_gate_without_gpu(lib):
+    S = binding.DecodeAttnSpec
+    assert binding.decode_attn_spec_check(S(softmax_scale=0.125)) == OK
+    assert binding.decode_attn_spec_check(S(causal=1, softmax_scale=0.125)) == OK
+    for field in ("has_alibi", "has_window_left", "has_window_right", "has_softcap"):
+        assert binding.decode_attn_spec_check(S(softmax_scale=0.125, **{field: 1})) == UNSUPPORTED
+    assert binding.decode_attn_spec_check(S(softmax_scale=math.inf)) == INVALID
+    assert binding.decode_attn_status_string(UNSUPPORTED)

@@ -10,7 +10,9 @@ _BINDING_NAMES = (
     "decode_attn_set_grid_limit", "decode_attn_read_device_error", "library_path",
     "load_library", "new_workspace", "run_case", "decode_attn_append_paged",
     "decode_attn_append_ring", "decode_attn_dense_device_len", "decode_attn_dense_mq",
-    "decode_attn_paged_mq",
+    "decode_attn_paged_mq", "decode_attn_check_wait_timeout", "decode_attn_spec_check",
+    "decode_attn_dense_spec", "decode_attn_dense_noalloc", "decode_attn_status_string",
+    "decode_attn_abi_version", "DecodeAttnSpec",
     "DA_VARIANT_DENSE", "DA_VARIANT_PAGED", "DA_VARIANT_SPARSE",
 )
 

@@ -19,6 +19,13 @@ _lock = threading.Lock()
 _lib = None
 
 
+class DecodeAttnSpec(ctypes.Structure):
+    """``decode_attn_spec``: the options of a decode-attention region (nonzero has_* = present)."""
+    _fields_ = [("has_alibi", ctypes.c_int), ("causal", ctypes.c_int),
+                ("has_window_left", ctypes.c_int), ("has_window_right", ctypes.c_int),
+                ("has_softcap", ctypes.c_int), ("softmax_scale", ctypes.c_float)]
+
+
 class DecodeAttnError(RuntimeError):
     def __init__(self, status: int, what: str, text: str):
         super().__init__(f"{what}: {text} (status {status})")
@@ -74,6 +81,13 @@ def load_library() -> ctypes.CDLL:
         lib.decode_attn_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         lib.decode_attn_check_wait_timeout.restype = i
         lib.decode_attn_check_wait_timeout.argtypes = [ctypes.c_uint32, vp]
+        lib.decode_attn_spec_check.restype = i
+        lib.decode_attn_spec_check.argtypes = [ctypes.POINTER(DecodeAttnSpec)]
+        lib.decode_attn_dense_spec.restype = i
+        lib.decode_attn_dense_spec.argtypes = [ctypes.POINTER(DecodeAttnSpec), vp, vp, vp, vp, i, i, i,
+                                               i, i64, i64, vp, sz, vp]
+        lib.decode_attn_dense_noalloc.restype = i
+        lib.decode_attn_dense_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i64, i64, f, vp]
         _lib = lib
         return lib
 
@@ -96,6 +110,42 @@ def _stream(stream, device):
 
 def abi_version() -> int:
     return load_library().decode_attn_abi_version()
+
+
+def decode_attn_abi_version() -> int:
+    return abi_version()
+
+
+def decode_attn_status_string(status: int) -> str:
+    return load_library().decode_attn_status_string(int(status)).decode()
+
+
+def decode_attn_spec_check(spec: DecodeAttnSpec) -> int:
+    """The gate: 0 (DA_OK) when these kernels can compute the region, else the refusing status
+    (DA_ERR_UNSUPPORTED for ALiBi / a window bound / a softcap).  Host only."""
+    return int(load_library().decode_attn_spec_check(ctypes.byref(spec) if spec is not None else None))
+
+
+def decode_attn_dense_spec(spec: DecodeAttnSpec, q, k, v, out, k_len: int, workspace, stream=None):
+    """decode_attn_spec_check, then decode_attn_dense with spec.softmax_scale."""
+    B, Hq, D = _dims_q(q)
+    Hkv, cap = k.shape[1], k.shape[2]
+    _check(load_library().decode_attn_dense_spec(
+        ctypes.byref(spec), _ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, D, cap, int(k_len),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream, q.device)),
+        "decode_attn_dense_spec")
+    return out
+
+
+def decode_attn_dense_noalloc(q, k, v, out, k_len: int, softmax_scale: float, stream=None):
+    """decode_attn_dense with the library-owned device scratch as its workspace (no allocation;
+    calls sharing the scratch must not overlap)."""
+    B, Hq, D = _dims_q(q)
+    Hkv, cap = k.shape[1], k.shape[2]
+    _check(load_library().decode_attn_dense_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, D, cap, int(k_len),
+        float(softmax_scale), _stream(stream, q.device)), "decode_attn_dense_noalloc")
+    return out
 
 
 def decode_attn_workspace_size(variant: int, B: int, Hq: int, Hkv: int, D: int, max_kv: int = 0) -> int:
