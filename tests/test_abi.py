@@ -145,17 +145,13 @@ def test_append_rejects(lib):
     assert ar(B=0) == OK
 
 
-class Spec(ctypes.Structure):
-    _fields_ = [("has_alibi", ctypes.c_int), ("causal", ctypes.c_int),
-                ("has_window_left", ctypes.c_int), ("has_window_right", ctypes.c_int),
-                ("has_softcap", ctypes.c_int), ("softmax_scale", ctypes.c_float)]
+Spec = binding.DecodeAttnSpec     # the ABI's decode_attn_spec layout
 
 
 def test_flash_spec_gate(lib):
     """Which options disqualify the flash arm (tests/golden/flash_spec_gate.json)."""
     import json
     rule = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "flash_spec_gate.json")))
-    lib.decode_attn_spec_check.argtypes = [ctypes.POINTER(Spec)]
     lib.decode_attn_spec_check.restype = ctypes.c_int
     assert lib.decode_attn_spec_check(ctypes.byref(Spec(softmax_scale=0.125))) == OK
     for f in rule["accepted_and_ignored"]:
