@@ -59,3 +59,11 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     status = fn(FAKE, FAKE, FAKE, FAKE, 1024, 64, 64, 128, 16, 8, 0.1, None)
     assert status == 3    # DA_ERR_WORKSPACE_TOO_SMALL, nothing launched
     assert B_.decode_attn_read_device_error() == 0
+
+
+def test_noalloc_binding_wrapper_matches_the_plain_call():
+    c = W.make_dense(2, 16, 4, 128, 600, 555, seed=161, device=DEV, k_scale=2.0)
+    ref = B_.run_case(c)
+    out = B_.decode_attn_dense_noalloc(c.q, c.k, c.v, torch.empty_like(ref), c.k_len, c.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
