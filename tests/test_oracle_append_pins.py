@@ -89,3 +89,18 @@ def test_ring_append_then_sparse_attention_sees_the_new_row():
     out = oracle.sparse(s.q, kp, vp, sel, s.scale)
     for b in range(B):
         np.testing.assert_array_equal(out[b], np.repeat(v_new[b].double().numpy(), Hq // Hkv, 0))
+
+
+def test_paged_slot_past_the_pool_writes_nothing():
+    """A slot at or past num_pages * page_size is skipped: the pool is the first 2 pages of a
+    3-page buffer, and the guard page after it must stay untouched."""
+    k_new = bits_of([[[7.0]], [[8.0]], [[9.0]]])                   # [T=3, Hkv=1, D=1]
+    buf_k = bits_of(np.full((3, 1, 2, 1), 5.0))
+    buf_v = bits_of(np.full((3, 1, 2, 1), 5.0))
+    kp, vp = buf_k[:2], buf_v[:2]                                  # C-contiguous views, 2 pages
+    oracle.append_paged(k_new, k_new, kp, vp, [1, 4, 5], inplace=True)
+    guard = np.full((1, 2, 1), 5.0)
+    for buf in (buf_k, buf_v):
+        vals = torch.from_numpy(buf.view(np.int16)).view(torch.bfloat16).float().numpy()
+        np.testing.assert_array_equal(vals[2], guard)             # slots 4, 5: page 2 untouched
+        assert vals[0, 0, 1, 0] == 7.0 and vals[0, 0, 0, 0] == 5.0 and (vals[1] == 5.0).all()
