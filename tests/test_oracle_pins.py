@@ -244,3 +244,22 @@ def test_rejects_bad_arguments():
         oracle.dense(c.q, c.k, c.v, 5, c.scale)            # k_len > capacity
     with pytest.raises(ValueError):
         oracle.dense(c.q, c.k, c.v, 2, c.scale, pairs=[8])  # pair index out of range
+
+
+def test_sparse_every_negative_index_is_skipped():
+    """Any negative entry (not only -1) and any entry >= pool_rows is skipped.  On the second
+    sequence a wrongly kept -2 or -1000 would read rows of the first sequence's pool (set to large
+    values here), so the result would change."""
+    B, Hq, Hkv, D, R = 2, 4, 1, 8, 16
+    g = torch.Generator().manual_seed(55)
+    q = torch.randn(B, Hq, 1, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Hkv, R, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Hkv, R, D, generator=g).to(torch.bfloat16)
+    k[0] = 40.0
+    v[0] = 1000.0
+    clean = torch.tensor([[0, 3, 5, -1, -1], [2, 7, 11, -1, -1]], dtype=torch.int32)
+    dirty = torch.tensor([[0, -2, 3, 5, -1000], [2, -2, 7, -1000, 11]], dtype=torch.int32)
+    over = torch.tensor([[0, 3, 5, 16, 99], [2, 7, 11, 16, 2 ** 30]], dtype=torch.int32)
+    ref = oracle.sparse(q, k, v, clean.numpy(), 0.3)
+    np.testing.assert_array_equal(oracle.sparse(q, k, v, dirty.numpy(), 0.3), ref)
+    np.testing.assert_array_equal(oracle.sparse(q, k, v, over.numpy(), 0.3), ref)
