@@ -36,9 +36,29 @@ DEFAULT_WORKLOAD = "dense_batched"
 KERNEL_SOURCES = {
     "decode": ["token_decode_attention_split_gb300/csrc/decode_kernel.cuh",
                "token_decode_attention_split_gb300/csrc/ptx.cuh"],
+    "sparse_tc": ["token_decode_attention_split_gb300/csrc/sparse_tc.cu",
+                  "token_decode_attention_split_gb300/csrc/decode_kernel.cuh",
+                  "token_decode_attention_split_gb300/csrc/ptx.cuh"],
     "append": ["token_decode_attention_split_gb300/csrc/append.cu",
                "token_decode_attention_split_gb300/csrc/ptx.cuh"],
 }
+
+
+def kernel_kind(cfg: dict) -> str:
+    """Which kernel a workload's timed call runs: "append", "sparse_tc" (sparse calls with 33..64
+    query heads per KV head at head dim 128 go to the tensor-core kernel, as the library
+    dispatches them) or "decode" (the mma.sync decode kernel)."""
+    if cfg["kind"] == "append":
+        return "append"
+    if cfg["kind"] == "sparse" and cfg["D"] == 128 and 32 < cfg["Hq"] // cfg["Hkv"] <= 64:
+        return "sparse_tc"
+    return "decode"
+
+
+def kernel_label(cfg: dict) -> str:
+    k = kernel_kind(cfg)
+    return {"append": "append_kernel", "sparse_tc": "sparse_tc_kernel"}.get(
+        k, f"decode_attn_kernel<{cfg['kind']}>")
 
 
 def code_only(src: str) -> str:
@@ -67,9 +87,9 @@ def code_only(src: str) -> str:
 
 def kernel_sha(kind: str = "decode") -> str:
     """First 16 hex digits of the sha256 of the code (comments and layout aside) of the sources
-    of the kernel a workload times."""
+    of the kernel a workload times (kind: a kernel_kind())."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES["append" if kind == "append" else "decode"]:
+    for f in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
             h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
@@ -93,7 +113,7 @@ def traffic_record(workload: str):
         with open(path) as f:
             d = json.load(f)
         rec = d.get(workload)
-        if rec and rec.get("kernel_sha") == kernel_sha(W.CONFIGS[workload]["kind"]):
+        if rec and rec.get("kernel_sha") == kernel_sha(kernel_kind(W.CONFIGS[workload])):
             return float(rec["bytes_per_launch"])
     except Exception:
         pass
@@ -560,8 +580,7 @@ def run_native(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": ("append_kernel" if c0.kind == "append"
-                                else f"decode_attn_kernel<{c0.kind}>"),
+                     "kernel": kernel_label({**W.CONFIGS[name], **OVERRIDES}),
                      "timing": "cuda graph of K calls",
                      "launch_us": round(launch_ms * 1e3, 2)},
         "clocks": clk,

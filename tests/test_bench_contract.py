@@ -39,3 +39,21 @@ def test_reference_line(workload):
         if k != "seed":
             assert cfg[k] == v
     assert cfg["algorithmic_bytes_per_call"] > 0
+
+
+def test_kernel_kind_follows_the_library_dispatch():
+    """The kernel whose sources key a workload's DRAM-traffic record: the sparse workload (64
+    query heads per KV head at D = 128) runs the tensor-core sparse kernel, whose hash covers
+    sparse_tc.cu as well as the shared headers."""
+    import bench
+    from token_decode_attention_split_gb300 import workloads as W
+    kinds = {name: bench.kernel_kind(cfg) for name, cfg in W.CONFIGS.items()}
+    assert kinds["sparse_selected"] == "sparse_tc"
+    assert kinds["append_paged"] == "append"
+    assert all(k == "decode" for n, k in kinds.items() if n.startswith(("dense", "paged")))
+    assert bench.kernel_kind(dict(kind="sparse", Hq=32, Hkv=1, D=128)) == "decode"   # G = 32
+    assert bench.kernel_kind(dict(kind="sparse", Hq=64, Hkv=1, D=64)) == "decode"    # D = 64
+    assert bench.kernel_kind(dict(kind="sparse", Hq=33, Hkv=1, D=128)) == "sparse_tc"
+    assert any("sparse_tc.cu" in f for f in bench.KERNEL_SOURCES["sparse_tc"])
+    assert bench.kernel_label(W.CONFIGS["sparse_selected"]) == "sparse_tc_kernel"
+    assert len({bench.kernel_sha(k) for k in bench.KERNEL_SOURCES}) == 3

@@ -21,8 +21,9 @@ CASES = [
     (2, 64, 8, 128, 1500, 1000, 64, 300),   # G = 8
     (2, 16, 1, 128, 900, 256, 8, 0),        # G = 16, exactly one chunk
     (2, 32, 1, 64, 800, 513, 8, 100),       # G = 32
-    (1, 48, 1, 128, 5000, 2048, 128, 512),  # G = 48: head groups of 32 and 16, two chunks
-    (2, 64, 1, 128, 9000, 5000, 128, 300),  # G = 64: two head groups, five chunks
+    (1, 48, 1, 128, 5000, 2048, 128, 512),  # G = 48: tensor-core kernel, four chunks
+    (2, 64, 1, 128, 9000, 5000, 128, 300),  # G = 64: tensor-core kernel, ten chunks
+    (2, 48, 1, 64, 3000, 1500, 32, 100),    # G = 48 at D = 64: head groups of 32 and 16
     (2, 16, 2, 64, 3000, 1100, 32, 50),     # G = 16: three chunks
 ]
 
@@ -68,7 +69,8 @@ def test_single_valid_entry_returns_that_row():
     assert torch.equal(out[1, :, 0], c.v_pool[1, 0, 5].expand(64, -1))
 
 
-@pytest.mark.parametrize("G,Hkv,D", [(64, 1, 128), (8, 2, 128), (4, 4, 64), (16, 1, 128)])
+@pytest.mark.parametrize("G,Hkv,D", [(64, 1, 128), (8, 2, 128), (4, 4, 64), (16, 1, 128),
+                                     (48, 1, 128), (64, 2, 128), (40, 1, 64)])
 def test_pads_are_bit_exactly_neutral(G, Hkv, D):
     """Per sequence: the padded fixed-width call and the call with the pads removed give the
     same bits; batched: appending more -1 pads changes no bit."""
@@ -84,6 +86,59 @@ def test_pads_are_bit_exactly_neutral(G, Hkv, D):
     wide = W.SparseCase(c.q, c.k_pool, c.v_pool, more.contiguous(), c.scale, c.B, c.Hq, c.Hkv,
                         c.D, c.pool_rows, c.n_valid_host)
     assert torch.equal(B_.run_case(wide), full)
+
+
+# ---- the tensor-core kernel (33..64 query heads per KV head at D = 128): CTA = (unit, chunk of
+# 512 entries) with every head of the unit
+
+TC_CASES = [
+    # B, Hq, Hkv, pool_rows, width, window, max_pad
+    (2, 64, 1, 2000, 1, 1, 0),        # one entry
+    (2, 64, 1, 2000, 64, 8, 0),       # one full tile
+    (2, 64, 1, 2000, 65, 8, 0),       # a tile and one row
+    (2, 64, 1, 2000, 511, 16, 0),     # chunk - 1
+    (2, 64, 1, 2000, 512, 16, 0),     # exactly one chunk
+    (2, 64, 1, 2000, 513, 16, 0),     # chunk + 1: a second chunk of one row
+    (3, 33, 1, 3000, 1100, 32, 90),   # G = 33: one live lane in the second softmax warp
+    (2, 80, 2, 3000, 900, 32, 400),   # G = 40, two units per sequence
+    (2, 128, 2, 4000, 1600, 64, 200), # G = 64, two units per sequence, four chunks
+]
+
+
+@pytest.mark.parametrize("cfg", TC_CASES, ids=lambda c: "B{}_Hq{}_Hkv{}_R{}_W{}".format(*c[:5]))
+def test_sparse_tensor_core_kernel_matches_oracle(cfg):
+    B, Hq, Hkv, R, width, window, max_pad = cfg
+    c = W.make_sparse(B, Hq, Hkv, 128, R, width, window, max_pad, seed=500 + width, device=DEV,
+                      poison_unselected=True)
+    out = B_.run_case(c)
+    assert_close(out_f64(out), oracle_for(c), f"tensor-core sparse {cfg}")
+
+
+def test_sparse_tensor_core_growing_scores_rescale():
+    """Scores that keep growing along the selection move the running maximum by far more than
+    the rescale threshold many times inside a chunk (the accumulator is rescaled in TMEM)."""
+    c = W.make_sparse(2, 64, 1, 128, 6000, 1500, 32, 0, seed=61, device=DEV)
+    for b in range(c.B):
+        n = c.n_valid_host[b]
+        idx = c.sel[b, :n].long()
+        f = (1.0 + torch.arange(n, device=DEV, dtype=torch.float32) / 24.0)[:, None]
+        c.k_pool[b, 0, idx] = (c.k_pool[b, 0, idx].float() * f).to(torch.bfloat16)
+    out = B_.run_case(c)
+    assert_close(out_f64(out), oracle_for(c), "growing scores")
+
+
+def test_sparse_tensor_core_pad_tiles_and_empty_chunk():
+    """Whole tiles of -1 at the start and inside a chunk, and a chunk with no valid entry (its
+    partial is empty and the merge skips it)."""
+    c = W.make_sparse(2, 64, 1, 128, 4000, 1600, 16, 0, seed=62, device=DEV)
+    sel = c.sel.clone()
+    sel[0, 0:128] = -1            # the first two tiles of chunk 0
+    sel[0, 300:364] = -1          # one tile inside chunk 0
+    sel[1, 512:1024] = -1         # chunk 1 entirely
+    sel[1, 1030] = 4000           # == pool_rows: skipped
+    c.sel = sel
+    out = B_.run_case(c)
+    assert_close(out_f64(out), oracle_for(c), "pad tiles / empty chunk")
 
 
 def test_sparse_width_zero_gives_zeros():

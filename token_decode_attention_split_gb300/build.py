@@ -14,7 +14,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libdecode_attn.so")
 SOURCES = ["api.cu", "kernels_dense.cu", "kernels_paged.cu", "kernels_paged_multi.cu",
-           "kernels_sparse.cu", "noalloc.cu", "append.cu", "wait_check.cu"]
+           "kernels_sparse.cu", "sparse_tc.cu", "noalloc.cu", "append.cu", "wait_check.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -177,13 +177,26 @@ int persistent_ctas(int dev) {
     return (lim > 0 && lim < sms) ? lim : sms;
 }
 
-// Sparse work split: query-head groups of 32 when G > 32, and chunks of 512 selection entries
-// per head group.  Both depend on G only, never on the width, B or the device.
-int sparse_head_groups(int G) { return G <= kSparseHeadGroup ? 1 : (G + kSparseHeadGroup - 1) / kSparseHeadGroup; }
-int sparse_segment_heads(int G) { return G <= kSparseHeadGroup ? G : kSparseHeadGroup; }
+// Sparse work split.  33..64 query heads per KV head at head dim 128 run on the tensor-core
+// kernel: one CTA per (unit, chunk of 512 entries) with all of the unit's heads.  Otherwise the
+// mma.sync kernel: query-head groups of 32 when G > 32, and chunks of 512 entries per head group.
+// Both depend on G and D only, never on the width, B or the device.
+bool sparse_uses_tc(int G, int D) { return D == 128 && G > kSparseHeadGroup && G <= 64; }
+int sparse_head_groups(int G, int D) {
+    if (sparse_uses_tc(G, D) || G <= kSparseHeadGroup) return 1;
+    return (G + kSparseHeadGroup - 1) / kSparseHeadGroup;
+}
+int sparse_segment_heads(int G, int D) {
+    return (sparse_uses_tc(G, D) || G <= kSparseHeadGroup) ? G : kSparseHeadGroup;
+}
 int sparse_padded_group(int G) { return G <= 8 ? 8 : G <= 16 ? 16 : 32; }
-long long sparse_chunk_keys(int G) { return static_cast<long long>(kSparseChunkUnit) * sparse_head_groups(G); }
-long long sparse_chunks(long long width, int G) { return (width + sparse_chunk_keys(G) - 1) / sparse_chunk_keys(G); }
+long long sparse_chunk_keys(int G, int D) {
+    if (sparse_uses_tc(G, D)) return sparse_tc_chunk();
+    return static_cast<long long>(kSparseChunkUnit) * sparse_head_groups(G, D);
+}
+long long sparse_chunks(long long width, int G, int D) {
+    return (width + sparse_chunk_keys(G, D) - 1) / sparse_chunk_keys(G, D);
+}
 
 }  // namespace
 
@@ -261,8 +274,8 @@ size_t decode_attn_workspace_size(int variant, int B, int Hq, int Hkv, int D, in
         segments = units + sms;
     } else if (variant == DA_VARIANT_SPARSE) {
         if (max_kv < 0) return 0;
-        const long long groups = units * sparse_head_groups(G);
-        return ws_layout(groups, groups * sparse_chunks(max_kv, G), sparse_segment_heads(G), D).total;
+        const long long groups = units * sparse_head_groups(G, D);
+        return ws_layout(groups, groups * sparse_chunks(max_kv, G, D), sparse_segment_heads(G, D), D).total;
     } else {
         return 0;
     }
@@ -529,15 +542,15 @@ da_status decode_attn_sparse(const void* q, const void* k_pool, const void* v_po
     if (pool_rows >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
     const long long units = static_cast<long long>(B) * Hkv;
     const int G = Hq / Hkv;
-    const long long groups = units * sparse_head_groups(G);
-    const long long chunks = sparse_chunks(width, G);
+    const long long groups = units * sparse_head_groups(G, D);
+    const long long chunks = sparse_chunks(width, G, D);
     if (groups * chunks >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (B == 0) return DA_OK;
     const int dev = current_device();
     if (dev < 0) return DA_ERR_CUDA;
     const int GP = sparse_padded_group(G);
-    const WsLayout w = ws_layout(groups, groups * chunks, sparse_segment_heads(G), D);
+    const WsLayout w = ws_layout(groups, groups * chunks, sparse_segment_heads(G, D), D);
     if (workspace_bytes < w.total) return DA_ERR_WORKSPACE_TOO_SMALL;
     if (width == 0) return zero_output(out, B, Hq, D, cs);
 
@@ -548,13 +561,17 @@ da_status decode_attn_sparse(const void* q, const void* k_pool, const void* v_po
     L.p.width = width;
     L.p.pool_rows = static_cast<int>(pool_rows);
     L.p.nchunks = static_cast<int>(chunks);
-    L.p.nhg = sparse_head_groups(G);
-    L.p.chunk_keys = static_cast<int>(sparse_chunk_keys(G));
-    L.p.seg_heads = sparse_segment_heads(G);
+    L.p.nhg = sparse_head_groups(G, D);
+    L.p.chunk_keys = static_cast<int>(sparse_chunk_keys(G, D));
+    L.p.seg_heads = sparse_segment_heads(G, D);
     L.p.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
     L.p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
     L.grid = static_cast<int>(groups * chunks);
     L.stream = cs;
+    if (sparse_uses_tc(G, D)) {
+        L.threads = sparse_tc_threads();
+        return launch_sparse_tc(L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+    }
     L.threads = Roles<kSparse>::kThreads;
     return launch_sparse(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }

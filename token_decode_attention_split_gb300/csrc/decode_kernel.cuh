@@ -80,7 +80,10 @@ struct Geometry {
     static constexpr int MT = kTileKeys / 16 / KS;              // 16-row m-tiles per warp
     static constexpr int KSTEPS = D / 16;                       // k-steps of S^T = K Q^T
     static constexpr int DT = D / 16;                           // 16-row d tiles of O^T
-    static constexpr int kMergeFloats = KS * GP * D + 2 * KS * GP + 4 * GP;   // + per-head stats
+    // merge slot rows are D + 4 floats apart, so the stash's stores (lanes 2 heads apart) fall
+    // in distinct banks
+    static constexpr int kMergeStride = D + 4;
+    static constexpr int kMergeFloats = KS * GP * kMergeStride + 2 * KS * GP + 4 * GP;   // + per-head stats
     static constexpr int kMiscBytes = 1024;                     // barriers, masks, flags
     static constexpr int kSchedBytes = (2 * kMaxPagedBatch + 2) * 4;
     static constexpr int kFixedBytes = kMergeFloats * 4 + kMiscBytes + kSchedBytes;
@@ -161,7 +164,7 @@ __device__ __forceinline__ SmemPtrs carve_smem(unsigned char* raw) {
     s.stages = base;
     unsigned char* p = base + Gm::kStages * Gm::kStageBytes;
     s.merge_o = reinterpret_cast<float*>(p);
-    s.merge_m = s.merge_o + Gm::KS * GP * D;
+    s.merge_m = s.merge_o + Gm::KS * GP * Gm::kMergeStride;
     s.merge_l = s.merge_m + Gm::KS * GP;
     s.head_inv = s.merge_l + Gm::KS * GP;
     s.head_lse = s.head_inv + GP;
@@ -532,8 +535,8 @@ struct ConsumerState {
                 }
 #pragma unroll
                 for (int dt = 0; dt < Gm::DT; ++dt) {
-                    sm.merge_o[slot * D + dt * 16 + gq] = o[dt][nt][hc];
-                    sm.merge_o[slot * D + dt * 16 + gq + 8] = o[dt][nt][hc + 2];
+                    sm.merge_o[slot * Gm::kMergeStride + dt * 16 + gq] = o[dt][nt][hc];
+                    sm.merge_o[slot * Gm::kMergeStride + dt * 16 + gq + 8] = o[dt][nt][hc + 2];
                 }
             }
     }
@@ -549,6 +552,12 @@ __device__ __forceinline__ bool group_sync(const SmemPtrs& sm, uint32_t& phase, 
         record_error(err, kErrWaitGroup);
     }
     return ok;
+}
+
+// acc + w * o, one rounding per component (the merges' accumulation step)
+__device__ __forceinline__ float4 fma4(float w, const float4& o, const float4& acc) {
+    return make_float4(__fmaf_rn(w, o.x, acc.x), __fmaf_rn(w, o.y, acc.y), __fmaf_rn(w, o.z, acc.z),
+                       __fmaf_rn(w, o.w, acc.w));
 }
 
 // Merges the nseg partial rows of unit U (workspace segments first_seg, first_seg + 1, ...) by
@@ -683,10 +692,7 @@ __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, 
                     if (w[u][j] == 0.f) continue;
                     const float ww = w[u][j];
                     if (started & (1u << j)) {
-                        acc[j].x += ww * o4[u][j].x;
-                        acc[j].y += ww * o4[u][j].y;
-                        acc[j].z += ww * o4[u][j].z;
-                        acc[j].w += ww * o4[u][j].w;
+                        acc[j] = fma4(ww, o4[u][j], acc[j]);
                     } else {
                         acc[j] = make_float4(ww * o4[u][j].x, ww * o4[u][j].y, ww * o4[u][j].z,
                                              ww * o4[u][j].w);
@@ -770,7 +776,7 @@ __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& 
         for (int k = 0; k < Gm::KS; ++k) {
             if (!((live >> k) & 1)) continue;
             const float w = sm.merge_m[k * GP + h];
-            const float4 o = *reinterpret_cast<const float4*>(sm.merge_o + (k * GP + h) * D + d);
+            const float4 o = *reinterpret_cast<const float4*>(sm.merge_o + (k * GP + h) * Gm::kMergeStride + d);
             if (first) {
                 O = make_float4(w * o.x, w * o.y, w * o.z, w * o.w);
                 first = false;

@@ -1,0 +1,598 @@
+// Sparse decode attention on the fifth-generation tensor cores (tcgen05), for units of 33..64
+// query heads per KV head at head dim 128.
+//
+// Why a second sparse kernel.  With more than 32 query heads per KV head the mma.sync kernel
+// splits the heads into groups of 32, so every selected row is gathered once per group, and its
+// warp-level MMAs bound the per-tile time.  Here one CTA holds all of the unit's heads: the group
+// is a real dense tile (S = Q K^T is 128 x 64 x 128 with the heads zero-padded to 128 rows), so
+// both products run as tcgen05.mma with the accumulators in tensor memory.
+//
+// Work split.  CTA = (unit u = (b, g), chunk of 512 selection entries); the chunk depends on
+// nothing but the kernel, so trailing -1 pads cannot move a chunk boundary.  Chunk pieces are
+// merged across CTAs by log-sum-exp exactly as in the mma.sync kernel (partial rows, a per-unit
+// counter, the last CTA merges in segment order).
+//
+// Inside a CTA (288 threads):
+//   warps 5-8  producers: gather the chunk's selected K and V rows with 16-byte cp.async into a
+//              ring of 4 stages (64 rows of K and of V each, 128-byte swizzle, rows outside
+//              [0, pool_rows) zero-filled); a stage's full barrier completes when every
+//              producer thread's copies for it have landed (cp.async.mbarrier.arrive), so
+//              the producers run ahead as far as the ring allows;
+//   warp 4     allocates 256 TMEM columns; one lane issues S(t) = Q K(t)^T into one of two
+//              64-column S buffers and O += P(t) V(t) into the 128-column O accumulator (after
+//              acquiring a stage it fences the generic proxy, in which cp.async wrote the rows,
+//              against the async proxy the MMAs read them through);
+//   warps 0-3  softmax: thread h owns query head h (TMEM lane h).  It reads its row of S(t),
+//              masks invalid rows, updates the running maximum and sum, writes its bf16 weights
+//              P(t) into a shared-memory P buffer (the A operand of the second MMA) and, at the
+//              end, normalises its O row and stores it (or its partial and log-sum-exp).
+// The running maximum used for the weights only moves when a tile's maximum exceeds it by more
+// than 8 (log2 units); the O row is rescaled in TMEM then.  Weights are therefore at most 2^8
+// before bf16 rounding, and the result is the same softmax with a different reference point.
+//
+// Safety.  Every wait is bounded (about one second) and raises the CTA's abort flag on timeout;
+// the MMA warp waits for all of its MMAs and for the softmax warps' last TMEM access before it
+// frees the tensor memory, on every path.
+#include "launch.h"
+
+namespace da {
+namespace {
+
+constexpr int kTcD = 128;
+constexpr int kTcM = 128;                        // MMA rows: the unit's query heads, zero-padded
+constexpr int kTcChunk = 512;                    // selection entries per CTA
+constexpr int kTcStages = 4;
+constexpr int kTcTileBytes = kTileKeys * kTcD * 2;     // one K (or V) tile, two 64-column halves
+constexpr int kTcStageBytes = 2 * kTcTileBytes;
+constexpr int kTcQBytes = kTcM * kTcD * 2;             // [2 halves][128 rows][128 B]
+constexpr int kTcPBytes = kTcM * kTileKeys * 2;        // [128 rows][128 B]: one tile's weights
+constexpr int kTcSoftmaxWarps = 4;
+constexpr int kTcMmaWarp = 4;
+constexpr int kTcProducerWarps = 4;
+constexpr int kTcThreads = 32 * (kTcSoftmaxWarps + 1 + kTcProducerWarps);
+constexpr uint32_t kTcCols = 256;                // TMEM: S buffers at columns 0 and 64, O at 128
+constexpr uint32_t kTcColO = 128;
+constexpr float kTcRescaleLog2 = 8.f;
+// tc_merge stages the rows of up to this many segments of 64 heads in the stage ring (4)
+constexpr int kTcMergeSegments = kTcStages * kTcStageBytes / (64 * kTcD * 4);
+constexpr int kTcRowStride = kTcD + 4;           // floats between staged O rows (bank spread)
+
+// shared-memory layout, from a 1024-byte aligned base
+constexpr int kOffQ = kTcStages * kTcStageBytes;
+constexpr int kOffP = kOffQ + kTcQBytes;
+constexpr int kOffBar = kOffP + 2 * kTcPBytes;
+constexpr int kOffIdx = kOffBar + 1024;
+constexpr int kTcSmemBytes = 1024 + kOffIdx + kTcChunk * 4;
+static_assert(kTcSmemBytes <= kSmemBudget, "shared memory");
+static_assert(kTcSoftmaxWarps * 32 == kConsumerThreads, "the merge runs on the softmax warps");
+static_assert(64 * kTcRowStride * 4 <= kTcStages * kTcStageBytes, "staged O rows");
+static_assert((kTcMergeSegments + 3) * 64 * 4 <= kTcQBytes, "merge weights");
+
+struct TcBars {
+    uint64_t full[kTcStages];    // stage's K and V rows landed (count: producer threads + 1)
+    uint64_t empty[kTcStages];   // stage's P.V completed (tcgen05.commit)
+    uint64_t s_ready[2];         // S buffer written (tcgen05.commit)
+    uint64_t s_free[2];          // S buffer read by the softmax warps (count: active warps)
+    uint64_t p_ready[2];         // P buffer written, O rescaled (count: active warps)
+    uint64_t pv_done[2];         // P.V of the tile with this parity completed (tcgen05.commit)
+    uint64_t q_ready;            // Q in shared memory (count: softmax threads)
+    uint64_t tmem_done;          // softmax warps finished with TMEM (count: softmax warps)
+    uint64_t drain;              // every MMA issued so far completed (tcgen05.commit)
+    uint64_t group;              // softmax-warp group barrier of the merge
+    uint64_t mrows;              // merge: a batch of partial rows landed (bulk copies)
+    uint64_t stage_mask[kTcStages];
+    uint32_t tmem_base;
+    int abort;
+    int last_flag;
+};
+static_assert(sizeof(TcBars) <= 1024, "barrier block");
+
+// A bounded wait whose outcome is the same on every lane of the warp (the tcgen05 loads and
+// stores that follow are warp-wide).
+__device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, volatile int* abort) {
+    return __all_sync(0xffffffffu, mbar_wait(b, parity, abort, kWaitLimitNs));
+}
+
+// Merges the nseg <= kTcMergeSegments partial rows of a unit of G <= 64 heads (workspace segments
+// first_seg, ...; one segment's rows are G * 512 contiguous bytes) by log-sum-exp in segment order
+// and stores its bf16 output rows; runs on the 128 softmax threads.  The arithmetic is
+// merge_unit's: the maximum over every segment's LSE, weights exp2(lse - max) of the live
+// segments summed in segment order from the first live one, rows accumulated in the same order
+// (first term w * o, then fma), the output acc * (1 / sum), and a head with a single live segment
+// copies that segment's row.  All rows land in `rows_sm` (the idle stage ring) by bulk copies that
+// thread 0 issues while the per-head weights are formed in `w_sm`; thread (warp w, lane c) then
+// takes float4 column c of heads w, w + 4, ..., eight heads at a time.  The caller has acquired
+// every segment's rows (the unit's counter) before the call.
+__device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, float* w_sm,
+                                      unsigned char* rows_sm, uint64_t* mrows, int hq0, int G,
+                                      int first_seg, int nseg, uint32_t& gphase) {
+    constexpr int D4 = kTcD / 4;
+    constexpr int kHeadsPerThread = 64 / kTcSoftmaxWarps;
+    constexpr int kPass = 8;                                 // heads per pass and thread
+    const int tid = threadIdx.x, wv = tid >> 5, c = tid & 31;
+    const size_t SH = static_cast<size_t>(p.seg_heads);
+    const uint32_t seg_bytes = static_cast<uint32_t>(G) * kTcD * 4;
+    const float* lse = p.part_lse + static_cast<size_t>(first_seg) * SH;
+    const float4* src = reinterpret_cast<const float4*>(p.part_o) + static_cast<size_t>(first_seg) * SH * D4;
+    const float4* rs = reinterpret_cast<const float4*>(rows_sm);
+    float* h_inv = w_sm + kTcMergeSegments * 64;             // [64]
+    int* h_live = reinterpret_cast<int*>(h_inv + 64);        // [64]
+    int* h_only = h_live + 64;                               // [64]
+    if (tid == 0) {
+        fence_proxy_async_global();
+        mbar_arrive_expect_tx(mrows, nseg * seg_bytes);
+        for (int k = 0; k < nseg; ++k)
+            bulk_load(rows_sm + k * seg_bytes, src + static_cast<size_t>(k) * SH * D4, seg_bytes, mrows);
+    }
+    if (tid < G) {
+        float l[kTcMergeSegments];
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int k = 0; k < kTcMergeSegments; ++k) {
+            l[k] = k < nseg ? __ldcg(lse + static_cast<size_t>(k) * SH + tid) : -CUDART_INF_F;
+            M = fmaxf(M, l[k]);
+        }
+        float L = 0.f;
+        int live = 0, only = 0;
+#pragma unroll
+        for (int k = 0; k < kTcMergeSegments; ++k) {
+            float w = 0.f;
+            if (l[k] != -CUDART_INF_F) {
+                w = fast_exp2(l[k] - M);
+                L = live ? L + w : w;
+                ++live;
+                only = k;
+            }
+            w_sm[k * 64 + tid] = w;
+        }
+        h_inv[tid] = live ? 1.0f / L : 0.f;
+        h_live[tid] = live;
+        h_only[tid] = only;
+    }
+    if (!mbar_wait(mrows, 0, sm.abort, kWaitLimitNs)) {
+        *sm.abort = 1;
+        record_error(p.err, kErrWaitFull);
+        // the copies in flight land before the CTA can exit
+        if (tid == 0 && !mbar_wait(mrows, 0, nullptr, kWaitLimitNs)) record_error(p.err, kErrDrain);
+        return false;
+    }
+    if (!group_sync(sm, gphase, p.err)) return false;   // weights visible
+    // not unrolled: the second pass runs the first pass's instructions, already in the cache
+#pragma unroll 1
+    for (int j0 = 0; j0 < kHeadsPerThread; j0 += kPass) {
+        float4 acc[kPass];
+        uint32_t started = 0;
+#pragma unroll
+        for (int j = 0; j < kPass; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        // branch-free so the loads of all heads issue together: a dead segment (w == 0) leaves
+        // the accumulator as it is, the first live one sets it to w * o
+        for (int k = 0; k < nseg; ++k) {
+            float w[kPass];
+            float4 o[kPass];
+#pragma unroll
+            for (int j = 0; j < kPass; ++j) {
+                const int hj = wv + kTcSoftmaxWarps * (j0 + j);
+                const int h = min(hj, G - 1);
+                w[j] = hj < G ? w_sm[k * 64 + h] : 0.f;
+                o[j] = rs[(k * G + h) * D4 + c];
+            }
+#pragma unroll
+            for (int j = 0; j < kPass; ++j) {
+                const float4 f = fma4(w[j], o[j], acc[j]);
+                const float4 m = make_float4(w[j] * o[j].x, w[j] * o[j].y, w[j] * o[j].z, w[j] * o[j].w);
+                const bool live = w[j] != 0.f;
+                const bool first = live && !((started >> j) & 1u);
+                acc[j] = first ? m : (live ? f : acc[j]);
+                started |= live ? (1u << j) : 0u;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPass; ++j) {
+            const int h = wv + kTcSoftmaxWarps * (j0 + j);
+            if (h >= G) continue;
+            const int live = h_live[h];
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (live == 1) {
+                v = rs[(h_only[h] * G + h) * D4 + c];
+            } else if (live > 1) {
+                const float inv = h_inv[h];
+                v = make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv);
+            }
+            *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(hq0 + h) * kTcD + 4 * c) =
+                make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+        }
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
+                 const Params p) {
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte aligned by an offset into the shared array, so accesses through `base` stay
+    // shared-memory accesses for the compiler
+    unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    TcBars& bar = *reinterpret_cast<TcBars*>(base + kOffBar);
+    int* sidx = reinterpret_cast<int*>(base + kOffIdx);
+    volatile int* abort = &bar.abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.G;
+    const int nact = (G + 31) >> 5;              // softmax warps that hold real heads
+
+    const int u = blockIdx.x / p.nchunks;
+    const int chunk = blockIdx.x - u * p.nchunks;
+    const int key0 = chunk * kTcChunk;
+    const int nkeys = min(kTcChunk, p.width - key0);
+    const int ntiles = (nkeys + kTileKeys - 1) / kTileKeys;
+    const int b = u / p.Hkv, g = u - b * p.Hkv;
+    const int hq0 = b * p.Hq + g * G;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(&bar.full[s], 32 * kTcProducerWarps + 1);
+            mbar_init(&bar.empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar.s_ready[i], 1);
+            mbar_init(&bar.s_free[i], nact);
+            mbar_init(&bar.p_ready[i], nact);
+            mbar_init(&bar.pv_done[i], 1);
+        }
+        mbar_init(&bar.q_ready, 32 * kTcSoftmaxWarps);
+        mbar_init(&bar.tmem_done, kTcSoftmaxWarps);
+        mbar_init(&bar.drain, 1);
+        mbar_init(&bar.group, kConsumerThreads);
+        mbar_init(&bar.mrows, 1);
+        bar.abort = 0;
+        bar.last_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == kTcMmaWarp) {
+        tmem_alloc(&bar.tmem_base, kTcCols);
+        tmem_relinquish_alloc_permit();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bar.tmem_base;
+    // nothing above touched global memory
+    grid_dependency_wait();
+    allow_dependent_launch();
+
+    if (warp > kTcMmaWarp) {
+        // ============================================================ producer warps
+        const int ptid = threadIdx.x - 32 * (kTcMmaWarp + 1);
+        const int pw = ptid >> 5;
+        const int* selrow = p.sel + static_cast<size_t>(b) * p.width + key0;
+        for (int i = ptid; i < nkeys; i += 32 * kTcProducerWarps) {
+            const int idx = __ldg(selrow + i);
+            sidx[i] = (idx >= 0 && idx < p.pool_rows) ? idx : -1;
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * kTcProducerWarps) : "memory");   // producers only
+        // lanes 0-15 copy the 16 chunks of a K row, lanes 16-31 those of the V row
+        const bool isv = lane >= 16;
+        const int c = lane & 15;
+        const __nv_bfloat16* pool = (isv ? p.v_pool : p.k_pool) +
+                                    static_cast<size_t>(u) * p.pool_rows * kTcD + c * 8;
+        constexpr int kRowsPerWarp = kTileKeys / kTcProducerWarps;
+        bool ok = true;
+        int t = 0;
+        for (; t < ntiles; ++t) {
+            const int s = t % kTcStages;
+            if (!mbar_wait(&bar.empty[s], ((t / kTcStages) & 1) ^ 1u, abort, kWaitLimitNs)) {
+                ok = false;
+                break;
+            }
+            const int l0 = t * kTileKeys;
+            if (pw == 0) {
+                const int i0 = l0 + lane, i1 = l0 + 32 + lane;
+                const bool v0 = i0 < nkeys && sidx[i0] >= 0;
+                const bool v1 = i1 < nkeys && sidx[i1] >= 0;
+                const uint64_t mask = static_cast<uint64_t>(__ballot_sync(0xffffffffu, v0)) |
+                                      (static_cast<uint64_t>(__ballot_sync(0xffffffffu, v1)) << 32);
+                if (lane == 0) bar.stage_mask[s] = mask;
+            }
+            unsigned char* tile = base + s * kTcStageBytes + (isv ? kTcTileBytes : 0);
+#pragma unroll 8
+            for (int r = pw * kRowsPerWarp; r < (pw + 1) * kRowsPerWarp; ++r) {
+                const int li = l0 + r;
+                const int idx = li < nkeys ? sidx[li] : -1;
+                const bool valid = idx >= 0;
+                cp_async_16(tile + tile_offset<2>(r, c, 6),
+                            pool + static_cast<size_t>(valid ? idx : 0) * kTcD, valid ? 16u : 0u);
+            }
+            cp_async_arrive_noinc(&bar.full[s]);
+            if (ptid == 0) mbar_arrive(&bar.full[s]);   // publishes the stage mask
+        }
+        if (!ok) {
+            // let every copy this thread issued land before the CTA can exit
+            cp_async_wait_all();
+            *abort = 1;
+            record_error(p.err, kErrWaitEmpty);
+        }
+        return;
+    }
+
+    if (warp == kTcMmaWarp) {
+        // ============================================================ MMA warp
+        if (lane == 0) {
+            constexpr uint32_t kIdS = umma_idesc_bf16(kTcM, kTileKeys, false);
+            constexpr uint32_t kIdO = umma_idesc_bf16(kTcM, kTcD, true);
+            const uint32_t q_s = smem_u32(base + kOffQ);
+            // S(t) = Q K(t)^T into S buffer t % 2: A = Q (K-major), B = the K tile (K-major)
+            auto issue_s = [&](int t) -> bool {
+                const int s = t % kTcStages, sb = t & 1;
+                if (!mbar_wait(&bar.full[s], (t / kTcStages) & 1, abort, kWaitLimitNs)) return false;
+                if (t >= 2 && !mbar_wait(&bar.s_free[sb], ((t - 2) >> 1) & 1, abort, kWaitLimitNs))
+                    return false;
+                fence_proxy_async_smem();
+                tc_fence_after_sync();
+                const uint32_t k_s = smem_u32(base + s * kTcStageBytes);
+#pragma unroll
+                for (int ks = 0; ks < kTcD / 16; ++ks) {
+                    const uint32_t off = (ks & 3) * 32u;   // 16 dims = 32 B into the swizzled row
+                    const uint64_t a = umma_desc_sw128(q_s + (ks >> 2) * (kTcM * 128) + off, 16, 1024);
+                    const uint64_t bd = umma_desc_sw128(k_s + (ks >> 2) * (kTileKeys * 128) + off, 16, 1024);
+                    umma_bf16(tmem + sb * kTileKeys, a, bd, kIdS, ks > 0 ? 1u : 0u);
+                }
+                umma_commit(&bar.s_ready[sb]);
+                return true;
+            };
+            bool ok = mbar_wait(&bar.q_ready, 0, abort, kWaitLimitNs);
+            if (ok) {
+                tc_fence_after_sync();
+                ok = issue_s(0);
+            }
+            for (int t = 0; ok && t < ntiles; ++t) {
+                if (t + 1 < ntiles && !issue_s(t + 1)) {
+                    ok = false;
+                    break;
+                }
+                const int s = t % kTcStages, pb = t & 1;
+                if (!mbar_wait(&bar.p_ready[pb], (t >> 1) & 1, abort, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                // O += P(t) V(t): A = P (K-major), B = the V tile (MN-major: dims contiguous)
+                const uint32_t p_s = smem_u32(base + kOffP + pb * kTcPBytes);
+                const uint32_t v_s = smem_u32(base + s * kTcStageBytes + kTcTileBytes);
+#pragma unroll
+                for (int ks = 0; ks < kTileKeys / 16; ++ks) {
+                    const uint64_t a = umma_desc_sw128(p_s + ks * 32, 16, 1024);
+                    const uint64_t bd = umma_desc_sw128(v_s + ks * 16 * 128, kTileKeys * 128, 1024);
+                    umma_bf16(tmem + kTcColO, a, bd, kIdO, (t > 0 || ks > 0) ? 1u : 0u);
+                }
+                umma_commit(&bar.pv_done[pb]);
+                umma_commit(&bar.empty[s]);
+            }
+            if (!ok) {
+                *abort = 1;
+                record_error(p.err, kErrWaitFull);
+            }
+            // every MMA issued above completes, and the softmax warps are done with TMEM,
+            // before the columns are freed
+            umma_commit(&bar.drain);
+            if (!mbar_wait(&bar.drain, 0, nullptr, kWaitLimitNs)) record_error(p.err, kErrDrain);
+            if (!mbar_wait(&bar.tmem_done, 0, nullptr, kWaitLimitNs)) record_error(p.err, kErrDrain);
+        }
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTcCols);
+        return;
+    }
+
+    // ================================================================ softmax warps
+    const int h = threadIdx.x;                   // query head of this thread = its TMEM lane
+    const bool warp_active = warp < nact;
+    const bool live = h < G;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    {
+        // Q rows of the unit (zero past G) in the A-operand layout; zero P rows past G
+        unsigned char* qs = base + kOffQ;
+        constexpr int kPer = kTcM * (kTcD / 8) / kConsumerThreads;   // 16-byte chunks per thread
+        uint4 v[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = threadIdx.x + k * kConsumerThreads, r = i >> 4, c = i & 15;
+            v[k] = r < G ? __ldg(reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(hq0 + r) * kTcD) + c)
+                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = threadIdx.x + k * kConsumerThreads, r = i >> 4, c = i & 15;
+            *reinterpret_cast<uint4*>(qs + (c >> 3) * (kTcM * 128) + r * 128 + (((c ^ r) & 7) << 4)) = v[k];
+        }
+        if (!live)
+            for (int i = 0; i < 2 * (kTileKeys / 8); ++i)
+                *reinterpret_cast<uint4*>(base + kOffP + (i >> 3) * kTcPBytes + h * 128 + (i & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar.q_ready);
+    }
+
+    float m_run = -CUDART_INF_F;   // reference maximum of the weights (log2 domain)
+    float l_run = 0.f;             // sum of the bf16-rounded weights
+    bool ok = true;
+    if (warp_active) {
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t % kTcStages, sb = t & 1;
+            if (!warp_wait(&bar.full[s], (t / kTcStages) & 1, abort) ||
+                !warp_wait(&bar.s_ready[sb], (t >> 1) & 1, abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            uint32_t sr[2][32];
+            tmem_ld32(t_lane + sb * kTileKeys, sr[0]);
+            tmem_ld32(t_lane + sb * kTileKeys + 32, sr[1]);
+            tmem_wait_ld();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.s_free[sb]);
+
+            // scores in the log2 domain, invalid rows at -inf
+            const uint64_t mask = bar.stage_mask[s];
+            float x[kTileKeys];
+            float mt = -CUDART_INF_F;
+#pragma unroll
+            for (int j = 0; j < kTileKeys; ++j) {
+                const float v = __uint_as_float(sr[j >> 5][j & 31]) * p.scale_log2;
+                x[j] = ((mask >> j) & 1ull) ? v : -CUDART_INF_F;
+                mt = fmaxf(mt, x[j]);
+            }
+            // move the reference maximum only on a large increase; O holds earlier weights
+            // (and needs the same rescale) only once some row has been seen
+            float alpha = 1.f;
+            if (mt > m_run + kTcRescaleLog2) {
+                alpha = fast_exp2(m_run - mt);   // 0 while m_run is -inf
+                m_run = mt;
+            }
+            const bool rescale = alpha != 1.f && l_run > 0.f;
+            if (__any_sync(0xffffffffu, rescale)) {
+                // the accumulator holds P.V up to tile t - 1 once that MMA has completed
+                if (!warp_wait(&bar.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const float a = rescale ? alpha : 1.f;
+#pragma unroll
+                for (int cb = 0; cb < kTcD / 32; ++cb) {
+                    uint32_t o[32];
+                    tmem_ld32(t_lane + kTcColO + cb * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * a);
+                    tmem_st32(t_lane + kTcColO + cb * 32, o);
+                }
+                tmem_wait_st();
+            }
+            l_run *= alpha;
+
+            // bf16 weights; the sum takes the rounded values
+            const float m_use = m_run == -CUDART_INF_F ? 0.f : m_run;
+            uint32_t pk[kTileKeys / 2];
+            float lsum = 0.f;
+#pragma unroll
+            for (int j = 0; j < kTileKeys / 2; ++j) {
+                const uint32_t w = live ? pack_bf16x2(fast_exp2(x[2 * j] - m_use),
+                                                      fast_exp2(x[2 * j + 1] - m_use))
+                                        : 0u;
+                lsum += bf16_lo_to_f32(w) + bf16_hi_to_f32(w);
+                pk[j] = w;
+            }
+            l_run += lsum;
+            // this P buffer was last read by the P.V of tile t - 2
+            if (t >= 2 && !warp_wait(&bar.pv_done[sb], ((t - 2) >> 1) & 1, abort)) {
+                ok = false;
+                break;
+            }
+            unsigned char* prow = base + kOffP + sb * kTcPBytes + h * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(prow + (((c ^ h) & 7) << 4)) =
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.p_ready[sb]);
+        }
+        if (ok && !warp_wait(&bar.pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort))
+            ok = false;
+    }
+
+    // The normalised O rows go through shared memory (row h of the idle stage ring,
+    // kTcRowStride floats apart) so that the global stores are coalesced: the output rows (one
+    // chunk) or this chunk's partial rows and LSEs.
+    const bool whole = p.nchunks == 1;
+    const size_t SH = static_cast<size_t>(p.seg_heads);
+    float* orow_sm = reinterpret_cast<float*>(base);
+    if (warp_active && ok) {
+        tc_fence_after_sync();
+        const bool empty = !(l_run > 0.f);
+        const float inv = empty ? 0.f : 1.0f / l_run;
+#pragma unroll
+        for (int cb = 0; cb < kTcD / 32; ++cb) {
+            uint32_t o[32];
+            tmem_ld32(t_lane + kTcColO + cb * 32, o);
+            tmem_wait_ld();
+            if (!live) continue;
+            float4* dst = reinterpret_cast<float4*>(orow_sm + h * kTcRowStride + cb * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                                     __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+        }
+        if (!whole && live)
+            p.part_lse[static_cast<size_t>(blockIdx.x) * SH + h] =
+                empty ? -CUDART_INF_F : m_run + fast_log2(l_run);
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar.tmem_done);
+    if (!ok) {
+        *abort = 1;
+        record_error(p.err, kErrWaitFull);
+        return;
+    }
+    SmemPtrs sm{};
+    sm.merge_o = reinterpret_cast<float*>(base);
+    sm.group = &bar.group;
+    sm.abort = abort;
+    sm.last_flag = &bar.last_flag;
+    uint32_t gphase = 0;
+    if (!group_sync(sm, gphase, p.err)) return;   // rows staged
+    {
+        // thread (warp w, lane c): float4 column c of heads w, w + 4, ...
+        const int wv = warp, c = lane;
+        for (int hh = wv; hh < G; hh += kTcSoftmaxWarps) {
+            const float4 v = *reinterpret_cast<const float4*>(orow_sm + hh * kTcRowStride + 4 * c);
+            if (whole)
+                *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(hq0 + hh) * kTcD + 4 * c) =
+                    make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+            else
+                *reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(blockIdx.x) * SH + hh) * kTcD + 4 * c) = v;
+        }
+    }
+    if (whole) return;
+
+    // cross-CTA merge of the unit's chunks (the stage ring is free now and serves as scratch)
+    Unit U{};
+    U.b = b;
+    U.g = g;
+    U.u = u;
+    U.hq0 = hq0;
+    U.nh = G;
+    U.cu = u;
+    // the group barrier orders every thread's partial-row stores before thread 0's release on
+    // the unit's counter; the CTA that completes the count acquires all chunks' rows there
+    if (!group_sync(sm, gphase, p.err)) return;
+    if (threadIdx.x == 0) {
+        const unsigned prev = atomic_add_acq_rel_gpu(p.counters + u);
+        *sm.last_flag = (prev == static_cast<unsigned>(p.nchunks - 1)) ? 1 : 0;
+    }
+    if (!group_sync(sm, gphase, p.err)) return;
+    if (*sm.last_flag) {
+        // the Q area holds the merge's per-segment weights and the stage ring its rows; more
+        // chunks take the general merge (same arithmetic; the stage ring is its scratch)
+        const bool ok_m = p.nchunks <= kTcMergeSegments
+                              ? tc_merge(p, sm, reinterpret_cast<float*>(base + kOffQ), base, &bar.mrows,
+                                         hq0, G, u * p.nchunks, p.nchunks, gphase)
+                              : merge_unit<kTcD, 64>(p, sm, U, u * p.nchunks, p.nchunks, gphase);
+        if (!ok_m) return;
+        if (threadIdx.x == 0) p.counters[u] = 0u;
+    }
+    group_sync(sm, gphase, p.err);
+}
+
+}  // namespace
+
+int sparse_tc_threads() { return kTcThreads; }
+int sparse_tc_chunk() { return kTcChunk; }
+
+cudaError_t launch_sparse_tc(const Launch& L) {
+    return launch_kernel(reinterpret_cast<const void*>(&sparse_tc_kernel), kTcSmemBytes, L);
+}
+
+}  // namespace da
