@@ -611,7 +611,6 @@ __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, 
 
     const int d4 = tid % D4, hq = tid / D4;
     float4 acc[NH];
-    uint32_t started = 0;
 #pragma unroll
     for (int j = 0; j < NH; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
 
@@ -688,17 +687,8 @@ __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, 
 #pragma unroll
             for (int u = 0; u < SU; ++u)
 #pragma unroll
-                for (int j = 0; j < NH; ++j) {
-                    if (w[u][j] == 0.f) continue;
-                    const float ww = w[u][j];
-                    if (started & (1u << j)) {
-                        acc[j] = fma4(ww, o4[u][j], acc[j]);
-                    } else {
-                        acc[j] = make_float4(ww * o4[u][j].x, ww * o4[u][j].y, ww * o4[u][j].z,
-                                             ww * o4[u][j].w);
-                        started |= 1u << j;
-                    }
-                }
+                for (int j = 0; j < NH; ++j)
+                    if (w[u][j] != 0.f) acc[j] = fma4(w[u][j], o4[u][j], acc[j]);
         }
         if (!group_sync(sm, gphase, p.err)) return false;
     }

@@ -98,8 +98,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, volatile
 // and stores its bf16 output rows; runs on the 128 softmax threads.  The arithmetic is
 // merge_unit's: the maximum over every segment's LSE, weights exp2(lse - max) of the live
 // segments summed in segment order from the first live one, rows accumulated in the same order
-// (first term w * o, then fma), the output acc * (1 / sum), and a head with a single live segment
-// copies that segment's row.  All rows land in `rows_sm` (the idle stage ring) by bulk copies that
+// by fma from zero, the output acc * (1 / sum), and a head with a single live segment copies that
+// segment's row.  All rows land in `rows_sm` (the idle stage ring) by bulk copies that
 // thread 0 issues while the per-head weights are formed in `w_sm`; thread (warp w, lane c) then
 // takes float4 column c of heads w, w + 4, ..., eight heads at a time.  The caller has acquired
 // every segment's rows (the unit's counter) before the call.
@@ -108,7 +108,7 @@ __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, fl
                                       int first_seg, int nseg, uint32_t& gphase) {
     constexpr int D4 = kTcD / 4;
     constexpr int kHeadsPerThread = 64 / kTcSoftmaxWarps;
-    constexpr int kPass = 8;                                 // heads per pass and thread
+    constexpr int kPass = 4;                                 // heads per pass and thread
     const int tid = threadIdx.x, wv = tid >> 5, c = tid & 31;
     const size_t SH = static_cast<size_t>(p.seg_heads);
     const uint32_t seg_bytes = static_cast<uint32_t>(G) * kTcD * 4;
@@ -157,49 +157,48 @@ __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, fl
         return false;
     }
     if (!group_sync(sm, gphase, p.err)) return false;   // weights visible
-    // not unrolled: the second pass runs the first pass's instructions, already in the cache
+    // Passes of kPass heads per thread.  Every load of a pass (the heads' statistics and all their
+    // segments' weights and rows) is independent of the others and predicated rather than
+    // branched around, so they are all in flight together.
 #pragma unroll 1
     for (int j0 = 0; j0 < kHeadsPerThread; j0 += kPass) {
-        float4 acc[kPass];
-        uint32_t started = 0;
+        int live[kPass], only[kPass];
+        float inv[kPass];
 #pragma unroll
-        for (int j = 0; j < kPass; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        // branch-free so the loads of all heads issue together: a dead segment (w == 0) leaves
-        // the accumulator as it is, the first live one sets it to w * o
-        for (int k = 0; k < nseg; ++k) {
-            float w[kPass];
-            float4 o[kPass];
+        for (int j = 0; j < kPass; ++j) {
+            const int h = min(wv + kTcSoftmaxWarps * (j0 + j), G - 1);
+            live[j] = h_live[h];
+            only[j] = h_only[h];
+            inv[j] = h_inv[h];
+        }
+        float w[kTcMergeSegments][kPass];
+        float4 o[kTcMergeSegments][kPass];
+#pragma unroll
+        for (int k = 0; k < kTcMergeSegments; ++k)
 #pragma unroll
             for (int j = 0; j < kPass; ++j) {
                 const int hj = wv + kTcSoftmaxWarps * (j0 + j);
                 const int h = min(hj, G - 1);
-                w[j] = hj < G ? w_sm[k * 64 + h] : 0.f;
-                o[j] = rs[(k * G + h) * D4 + c];
+                const int kk = min(k, nseg - 1);
+                w[k][j] = (k < nseg && hj < G) ? w_sm[kk * 64 + h] : 0.f;
+                o[k][j] = rs[(kk * G + h) * D4 + c];
             }
-#pragma unroll
-            for (int j = 0; j < kPass; ++j) {
-                const float4 f = fma4(w[j], o[j], acc[j]);
-                const float4 m = make_float4(w[j] * o[j].x, w[j] * o[j].y, w[j] * o[j].z, w[j] * o[j].w);
-                const bool live = w[j] != 0.f;
-                const bool first = live && !((started >> j) & 1u);
-                acc[j] = first ? m : (live ? f : acc[j]);
-                started |= live ? (1u << j) : 0u;
-            }
-        }
 #pragma unroll
         for (int j = 0; j < kPass; ++j) {
-            const int h = wv + kTcSoftmaxWarps * (j0 + j);
-            if (h >= G) continue;
-            const int live = h_live[h];
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (live == 1) {
-                v = rs[(h_only[h] * G + h) * D4 + c];
-            } else if (live > 1) {
-                const float inv = h_inv[h];
-                v = make_float4(acc[j].x * inv, acc[j].y * inv, acc[j].z * inv, acc[j].w * inv);
+            // segment order; a dead segment (w == 0) leaves the accumulator as it is
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kTcMergeSegments; ++k) {
+                const float4 f = fma4(w[k][j], o[k][j], acc);
+                acc = w[k][j] != 0.f ? f : acc;
             }
-            *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(hq0 + h) * kTcD + 4 * c) =
-                make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+            const int h = wv + kTcSoftmaxWarps * (j0 + j);
+            const float4 single = rs[(only[j] * G + min(h, G - 1)) * D4 + c];
+            const float4 scaled = make_float4(acc.x * inv[j], acc.y * inv[j], acc.z * inv[j], acc.w * inv[j]);
+            const float4 v = live[j] == 1 ? single : (live[j] > 1 ? scaled : make_float4(0.f, 0.f, 0.f, 0.f));
+            if (h < G)
+                *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(hq0 + h) * kTcD + 4 * c) =
+                    make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
         }
     }
     return true;
