@@ -159,8 +159,9 @@ template <int D, int GP>
 __device__ __forceinline__ SmemPtrs carve_smem(unsigned char* raw) {
     using Gm = Geometry<D, GP>;
     SmemPtrs s;
-    unsigned char* base = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned by an offset into the shared array, so accesses through these pointers
+    // stay shared-memory accesses for the compiler
+    unsigned char* base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
     s.stages = base;
     unsigned char* p = base + Gm::kStages * Gm::kStageBytes;
     s.merge_o = reinterpret_cast<float*>(p);
