@@ -171,7 +171,7 @@ __device__ __forceinline__ SmemPtrs carve_smem(unsigned char* raw) {
     s.head_lse = s.head_inv + GP;
     s.head_live = reinterpret_cast<int*>(s.head_lse + GP);
     p += Gm::kMergeFloats * 4;
-    p = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15));
+    p += (16u - (smem_u32(p) & 15u)) & 15u;
     s.full = reinterpret_cast<uint64_t*>(p);
     s.empty = s.full + 8;
     s.group = s.empty + 8;
