@@ -58,6 +58,13 @@ struct Roles {
     static constexpr int kThreads = kConsumerThreads + 32 * kProducerWarps;
 };
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// A bounded wait executed by every lane of a warp whose outcome is the same on every lane: each
+// lane's limit runs on its own clock, and what follows a wait (a ballot, a shuffle, a warp-wide
+// MMA or load) needs all 32 lanes, so on a timeout the whole warp gives up together.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, kWaitLimitNs));
+}
 constexpr int kSparseHeadGroup = 32;         // query heads per CTA when a group is split
 constexpr int kSparseChunkUnit = 512;         // sparse chunk = 512 entries per head group
 constexpr int kMaxPagedBatch = 1024;
@@ -543,10 +550,11 @@ struct ConsumerState {
     }
 };
 
-// Consumer-group barrier (128 threads) on an mbarrier, bounded.
+// Consumer-group barrier (128 threads) on an mbarrier, bounded; every lane of a warp returns the
+// same outcome.
 __device__ __forceinline__ bool group_sync(const SmemPtrs& sm, uint32_t& phase, unsigned* err) {
     mbar_arrive(sm.group);
-    const bool ok = mbar_wait(sm.group, phase, sm.abort, kWaitLimitNs);
+    const bool ok = mbar_wait_warp(sm.group, phase, sm.abort);
     phase ^= 1u;
     if (!ok) {
         *sm.abort = 1;
@@ -926,7 +934,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             for (int t = t0; t < t1 && ok; ++t, ++it) {
                 const int s = it % S;
                 const uint32_t ph = (it / S) & 1;
-                if (!mbar_wait(sm.empty + s, ph ^ 1u, sm.abort, kWaitLimitNs)) { ok = false; break; }
+                if (!mbar_wait_warp(sm.empty + s, ph ^ 1u, sm.abort)) { ok = false; break; }
                 const int l0 = t * kTileKeys - sp_key0;
                 const int i0 = l0 + lane, i1 = l0 + 32 + lane;
                 const int idx0 = i0 < sp_nkeys ? sidx[i0] : -1;
@@ -983,7 +991,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 for (; t < tend; t += NPW, it += NPW) {
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1;
-                    if (!mbar_wait(sm.empty + s, ph ^ 1u, sm.abort, kWaitLimitNs)) { ok = false; break; }
+                    if (!mbar_wait_warp(sm.empty + s, ph ^ 1u, sm.abort)) { ok = false; break; }
                     const int j = t - U.base;
                     const int key0 = j * TK;
                     const int nvalid = min(TK, U.len - key0);
@@ -1124,7 +1132,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         for (int t = t0; t < t1; ++t, ++it) {
             const int s = it % S;
             const uint32_t ph = (it / S) & 1;
-            if (!mbar_wait(sm.full + s, ph, sm.abort, kWaitLimitNs)) {
+            if (!mbar_wait_warp(sm.full + s, ph, sm.abort)) {
                 *sm.abort = 1;
                 record_error(p.err, kErrWaitFull);
                 return;
@@ -1157,7 +1165,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         for (; t < tend; ++t, ++it) {
             const int s = it % S;
             const uint32_t ph = (it / S) & 1;
-            if (!mbar_wait(sm.full + s, ph, sm.abort, kWaitLimitNs)) {
+            if (!mbar_wait_warp(sm.full + s, ph, sm.abort)) {
                 *sm.abort = 1;
                 record_error(p.err, kErrWaitFull);
                 return;

@@ -87,12 +87,6 @@ struct TcBars {
 };
 static_assert(sizeof(TcBars) <= 1024, "barrier block");
 
-// A bounded wait whose outcome is the same on every lane of the warp (the tcgen05 loads and
-// stores that follow are warp-wide).
-__device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, volatile int* abort) {
-    return __all_sync(0xffffffffu, mbar_wait(b, parity, abort, kWaitLimitNs));
-}
-
 // Merges the nseg <= kTcMergeSegments partial rows of a unit of G <= 64 heads (workspace segments
 // first_seg, ...; one segment's rows are G * 512 contiguous bytes) by log-sum-exp in segment order
 // and stores its bf16 output rows; runs on the 128 softmax threads.  The arithmetic is
@@ -149,7 +143,7 @@ __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, fl
         h_live[tid] = live;
         h_only[tid] = only;
     }
-    if (!mbar_wait(mrows, 0, sm.abort, kWaitLimitNs)) {
+    if (!mbar_wait_warp(mrows, 0, sm.abort)) {
         *sm.abort = 1;
         record_error(p.err, kErrWaitFull);
         // the copies in flight land before the CTA can exit
@@ -278,7 +272,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
         int t = 0;
         for (; t < ntiles; ++t) {
             const int s = t % kTcStages;
-            if (!mbar_wait(&bar.empty[s], ((t / kTcStages) & 1) ^ 1u, abort, kWaitLimitNs)) {
+            if (!mbar_wait_warp(&bar.empty[s], ((t / kTcStages) & 1) ^ 1u, abort)) {
                 ok = false;
                 break;
             }
@@ -416,8 +410,8 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
     if (warp_active) {
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % kTcStages, sb = t & 1;
-            if (!warp_wait(&bar.full[s], (t / kTcStages) & 1, abort) ||
-                !warp_wait(&bar.s_ready[sb], (t >> 1) & 1, abort)) {
+            if (!mbar_wait_warp(&bar.full[s], (t / kTcStages) & 1, abort) ||
+                !mbar_wait_warp(&bar.s_ready[sb], (t >> 1) & 1, abort)) {
                 ok = false;
                 break;
             }
@@ -450,7 +444,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
             const bool rescale = alpha != 1.f && l_run > 0.f;
             if (__any_sync(0xffffffffu, rescale)) {
                 // the accumulator holds P.V up to tile t - 1 once that MMA has completed
-                if (!warp_wait(&bar.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort)) {
+                if (!mbar_wait_warp(&bar.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort)) {
                     ok = false;
                     break;
                 }
@@ -483,7 +477,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
             }
             l_run += lsum;
             // this P buffer was last read by the P.V of tile t - 2
-            if (t >= 2 && !warp_wait(&bar.pv_done[sb], ((t - 2) >> 1) & 1, abort)) {
+            if (t >= 2 && !mbar_wait_warp(&bar.pv_done[sb], ((t - 2) >> 1) & 1, abort)) {
                 ok = false;
                 break;
             }
@@ -497,7 +491,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.p_ready[sb]);
         }
-        if (ok && !warp_wait(&bar.pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort))
+        if (ok && !mbar_wait_warp(&bar.pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort))
             ok = false;
     }
 
