@@ -168,3 +168,14 @@ def test_sparse_named_workload():
 
 def test_no_device_error_recorded():
     assert B_.decode_attn_read_device_error() == 0
+
+
+@pytest.mark.parametrize("B,Hkv,width", [(80, 1, 1100), (48, 2, 700)])
+def test_sparse_tensor_core_kernel_several_waves(B, Hkv, width):
+    """More CTAs than SMs (240 and 192 CTAs of one per SM): later CTAs allocate tensor memory on
+    SMs whose earlier CTAs have freed it; every output row against the oracle."""
+    c = W.make_sparse(B, 64 * Hkv, Hkv, 128, 1500, width, 16, 150, seed=600 + B, device=DEV,
+                      poison_unselected=True)
+    out = B_.run_case(c)
+    assert_close(out_f64(out), oracle_for(c), f"tensor-core sparse, {B} sequences")
+    assert B_.decode_attn_read_device_error() == 0

@@ -506,16 +506,23 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
         const bool empty = !(l_run > 0.f);
         const float inv = empty ? 0.f : 1.0f / l_run;
 #pragma unroll
-        for (int cb = 0; cb < kTcD / 32; ++cb) {
-            uint32_t o[32];
-            tmem_ld32(t_lane + kTcColO + cb * 32, o);
+        for (int cb = 0; cb < kTcD / 32; cb += 2) {
+            // two 32-column loads in flight per wait
+            uint32_t o[2][32];
+            tmem_ld32(t_lane + kTcColO + cb * 32, o[0]);
+            tmem_ld32(t_lane + kTcColO + (cb + 1) * 32, o[1]);
             tmem_wait_ld();
             if (!live) continue;
-            float4* dst = reinterpret_cast<float4*>(orow_sm + h * kTcRowStride + cb * 32);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
-                                     __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+            for (int half = 0; half < 2; ++half) {
+                float4* dst = reinterpret_cast<float4*>(orow_sm + h * kTcRowStride + (cb + half) * 32);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    dst[j] = make_float4(__uint_as_float(o[half][4 * j]) * inv,
+                                         __uint_as_float(o[half][4 * j + 1]) * inv,
+                                         __uint_as_float(o[half][4 * j + 2]) * inv,
+                                         __uint_as_float(o[half][4 * j + 3]) * inv);
+            }
         }
         if (!whole && live)
             p.part_lse[static_cast<size_t>(blockIdx.x) * SH + h] =
@@ -537,15 +544,23 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
     uint32_t gphase = 0;
     if (!group_sync(sm, gphase, p.err)) return;   // rows staged
     {
-        // thread (warp w, lane c): float4 column c of heads w, w + 4, ...
+        // thread (warp w, lane c): float4 column c of heads w, w + 4, ...; a fixed trip count, so
+        // all sixteen shared-memory loads are in flight before the stores
         const int wv = warp, c = lane;
-        for (int hh = wv; hh < G; hh += kTcSoftmaxWarps) {
-            const float4 v = *reinterpret_cast<const float4*>(orow_sm + hh * kTcRowStride + 4 * c);
+        constexpr int kPer = 64 / kTcSoftmaxWarps;
+        float4 v[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+            v[j] = *reinterpret_cast<const float4*>(orow_sm + min(wv + kTcSoftmaxWarps * j, G - 1) * kTcRowStride + 4 * c);
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int hh = wv + kTcSoftmaxWarps * j;
+            if (hh >= G) continue;
             if (whole)
                 *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(hq0 + hh) * kTcD + 4 * c) =
-                    make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+                    make_uint2(pack_bf16x2(v[j].x, v[j].y), pack_bf16x2(v[j].z, v[j].w));
             else
-                *reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(blockIdx.x) * SH + hh) * kTcD + 4 * c) = v;
+                *reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(blockIdx.x) * SH + hh) * kTcD + 4 * c) = v[j];
         }
     }
     if (whole) return;
