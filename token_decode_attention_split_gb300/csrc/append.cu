@@ -5,9 +5,10 @@
 //   decode_attn_append_ring   "AttnV41" (attn_v41), method decode_body: the window ring write at
 //                             pos % window, the position read on the device.
 // Both are plain HBM-bound copies: one warp moves one new row (K and V of every KV head) with
-// 16-byte loads issued in batches before their stores, so a warp waits on memory about twice per
-// row (its slot word, then the row's data); the slot or position is read on the device and never
-// validated by a sync.
+// 16-byte loads issued in batches before their stores; the first batch of a row's data is
+// requested together with its slot word (the loads do not depend on it), so a warp waits on
+// memory about once per row.  The slot or position is read on the device and never validated by
+// a sync.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -62,9 +63,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
     const int half = a.Hkv * a.chunks;    // 16-byte chunks of one new row's K (or V), all heads
     for (int64_t row = blockIdx.x * (kAppendThreads / 32) + (threadIdx.x >> 5); row < a.rows;
          row += warps) {
-        int64_t base, head_stride;
-        if (!dest_rows(a, row, base, head_stride)) continue;
         const int64_t src0 = row * half;
+        int64_t base = 0, head_stride = 0;
         for (int c0 = 0; c0 < 2 * half; c0 += 32 * kAppendBatch) {
             uint4 x[kAppendBatch];
 #pragma unroll
@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs
                     x[i] = __ldg((isv ? a.v_new : a.k_new) + src0 + (isv ? c - half : c));
                 }
             }
+            // the slot word, requested after the first batch: a skipped row stores nothing
+            if (c0 == 0 && !dest_rows(a, row, base, head_stride)) break;
 #pragma unroll
             for (int i = 0; i < kAppendBatch; ++i) {
                 const int c = c0 + i * 32 + lane;
