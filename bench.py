@@ -46,11 +46,11 @@ KERNEL_SOURCES = {
 
 def kernel_kind(cfg: dict) -> str:
     """Which kernel a workload's timed call runs: "append", "sparse_tc" (sparse calls with 33..64
-    query heads per KV head at head dim 128 go to the tensor-core kernel, as the library
-    dispatches them) or "decode" (the mma.sync decode kernel)."""
+    query heads per KV head go to the tensor-core kernel, as the library dispatches them) or
+    "decode" (the mma.sync decode kernel)."""
     if cfg["kind"] == "append":
         return "append"
-    if cfg["kind"] == "sparse" and cfg["D"] == 128 and 32 < cfg["Hq"] // cfg["Hkv"] <= 64:
+    if cfg["kind"] == "sparse" and 32 < cfg["Hq"] // cfg["Hkv"] <= 64:
         return "sparse_tc"
     return "decode"
 

@@ -155,10 +155,9 @@ da_status decode_attn_paged_mq(const void *q, const void *k_pool, const void *v_
  * entry); a -1 entry adds an exact zero to the denominator and nothing to the output.
  * Appending -1 pads to a selection leaves every output bit unchanged: the work is split into
  * chunks whose size depends on G = Hq / Hkv and D only, not on the width, B or the device.
- * 33 <= G <= 64 at D = 128 runs on the fifth-generation tensor cores (tcgen05, accumulators in
- * tensor memory), one CTA per (sequence and KV head, chunk of 512 entries) holding all G heads;
- * every other shape runs on warp-level MMAs with chunks of 512 * ceil(G / 32) entries per group
- * of at most 32 heads.
+ * 33 <= G <= 64 runs on the fifth-generation tensor cores (tcgen05, accumulators in tensor
+ * memory), one CTA per (sequence and KV head, chunk of 512 entries) holding all G heads; G <= 32
+ * runs on warp-level MMAs with chunks of 512 entries.
  *   1 <= pool_rows < 2^31; width >= 0 (width = 0 writes zeros).
  */
 da_status decode_attn_sparse(const void *q, const void *k_pool, const void *v_pool, void *out,

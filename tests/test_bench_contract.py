@@ -52,7 +52,7 @@ def test_kernel_kind_follows_the_library_dispatch():
     assert kinds["append_paged"] == "append"
     assert all(k == "decode" for n, k in kinds.items() if n.startswith(("dense", "paged")))
     assert bench.kernel_kind(dict(kind="sparse", Hq=32, Hkv=1, D=128)) == "decode"   # G = 32
-    assert bench.kernel_kind(dict(kind="sparse", Hq=64, Hkv=1, D=64)) == "decode"    # D = 64
+    assert bench.kernel_kind(dict(kind="sparse", Hq=64, Hkv=1, D=64)) == "sparse_tc"
     assert bench.kernel_kind(dict(kind="sparse", Hq=33, Hkv=1, D=128)) == "sparse_tc"
     assert any("sparse_tc.cu" in f for f in bench.KERNEL_SOURCES["sparse_tc"])
     assert bench.kernel_label(W.CONFIGS["sparse_selected"]) == "sparse_tc_kernel"

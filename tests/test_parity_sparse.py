@@ -23,7 +23,7 @@ CASES = [
     (2, 32, 1, 64, 800, 513, 8, 100),       # G = 32
     (1, 48, 1, 128, 5000, 2048, 128, 512),  # G = 48: tensor-core kernel, four chunks
     (2, 64, 1, 128, 9000, 5000, 128, 300),  # G = 64: tensor-core kernel, ten chunks
-    (2, 48, 1, 64, 3000, 1500, 32, 100),    # G = 48 at D = 64: head groups of 32 and 16
+    (2, 48, 1, 64, 3000, 1500, 32, 100),    # G = 48 at D = 64: tensor-core kernel, three chunks
     (2, 16, 2, 64, 3000, 1100, 32, 50),     # G = 16: three chunks
 ]
 
@@ -179,3 +179,34 @@ def test_sparse_tensor_core_kernel_several_waves(B, Hkv, width):
     out = B_.run_case(c)
     assert_close(out_f64(out), oracle_for(c), f"tensor-core sparse, {B} sequences")
     assert B_.decode_attn_read_device_error() == 0
+
+
+TC64_CASES = [
+    # B, Hq, Hkv, pool_rows, width, window, max_pad  (head dim 64)
+    (2, 64, 1, 2000, 1, 1, 0),
+    (2, 64, 1, 2000, 65, 8, 0),
+    (2, 64, 1, 2000, 513, 16, 0),
+    (3, 33, 1, 3000, 1100, 32, 90),
+    (2, 128, 2, 4000, 1600, 64, 200),
+    (60, 40, 1, 1500, 1100, 16, 150),   # 180 CTAs: more than one wave
+]
+
+
+@pytest.mark.parametrize("cfg", TC64_CASES, ids=lambda c: "B{}_Hq{}_Hkv{}_R{}_W{}".format(*c[:5]))
+def test_sparse_tensor_core_kernel_d64_matches_oracle(cfg):
+    B, Hq, Hkv, R, width, window, max_pad = cfg
+    c = W.make_sparse(B, Hq, Hkv, 64, R, width, window, max_pad, seed=700 + width, device=DEV,
+                      poison_unselected=True)
+    out = B_.run_case(c)
+    assert_close(out_f64(out), oracle_for(c), f"tensor-core sparse D=64 {cfg}")
+
+
+def test_sparse_tensor_core_d64_growing_scores_rescale():
+    c = W.make_sparse(2, 48, 1, 64, 6000, 1500, 32, 0, seed=63, device=DEV)
+    for b in range(c.B):
+        n = c.n_valid_host[b]
+        idx = c.sel[b, :n].long()
+        f = (1.0 + torch.arange(n, device=DEV, dtype=torch.float32) / 16.0)[:, None]
+        c.k_pool[b, 0, idx] = (c.k_pool[b, 0, idx].float() * f).to(torch.bfloat16)
+    out = B_.run_case(c)
+    assert_close(out_f64(out), oracle_for(c), "growing scores, D=64")

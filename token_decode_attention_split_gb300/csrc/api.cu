@@ -177,11 +177,13 @@ int persistent_ctas(int dev) {
     return (lim > 0 && lim < sms) ? lim : sms;
 }
 
-// Sparse work split.  33..64 query heads per KV head at head dim 128 run on the tensor-core
-// kernel: one CTA per (unit, chunk of 512 entries) with all of the unit's heads.  Otherwise the
-// mma.sync kernel: query-head groups of 32 when G > 32, and chunks of 512 entries per head group.
-// Both depend on G and D only, never on the width, B or the device.
-bool sparse_uses_tc(int G, int D) { return D == 128 && G > kSparseHeadGroup && G <= 64; }
+// Sparse work split.  33..64 query heads per KV head run on the tensor-core kernel: one CTA per
+// (unit, chunk of 512 entries) with all of the unit's heads.  Otherwise the mma.sync kernel:
+// chunks of 512 entries for the (at most 32) heads of a unit.  Both depend on G and D only,
+// never on the width, B or the device.
+bool sparse_uses_tc(int G, int D) {
+    return (D == 64 || D == 128) && G > kSparseHeadGroup && G <= 64;
+}
 int sparse_head_groups(int G, int D) {
     if (sparse_uses_tc(G, D) || G <= kSparseHeadGroup) return 1;
     return (G + kSparseHeadGroup - 1) / kSparseHeadGroup;
@@ -570,7 +572,7 @@ da_status decode_attn_sparse(const void* q, const void* k_pool, const void* v_po
     L.stream = cs;
     if (sparse_uses_tc(G, D)) {
         L.threads = sparse_tc_threads();
-        return launch_sparse_tc(L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+        return launch_sparse_tc(D, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
     }
     L.threads = Roles<kSparse>::kThreads;
     return launch_sparse(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;

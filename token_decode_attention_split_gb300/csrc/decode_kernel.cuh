@@ -574,7 +574,9 @@ __device__ __forceinline__ float4 fma4(float w, const float4& o, const float4& a
 // the 128 consumer threads of the CTA that completed the unit and uses the merge area of shared
 // memory as scratch: the partial LSEs are read once, coalesced, into shared memory; each thread
 // then owns float4 slices of the output and keeps several partial rows in flight.
-template <int D, int GP>
+// kNoPrefetch: never issue the row loads ahead (fewer registers, for callers whose register
+// budget is tight; same arithmetic).
+template <int D, int GP, bool kNoPrefetch = false>
 __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, const Unit& U,
                                            int first_seg, int nseg, uint32_t& gphase) {
     using Gm = Geometry<D, GP>;
@@ -626,7 +628,7 @@ __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, 
     // Few segments (the usual case): issue the partial-row loads now, together with the LSE
     // loads below, so the merge costs one L2 round trip instead of two.
     // (Not for 64-head groups, whose 16 rows per thread would not fit the register budget.)
-    constexpr bool kPrefetch = NH <= 8;
+    constexpr bool kPrefetch = NH <= 8 && !kNoPrefetch;
     constexpr int PU = kPrefetch ? SU : 1, PH = kPrefetch ? NH : 1;
     const bool prefetched = kPrefetch && one_batch && nseg <= SU;
     float4 pre[PU][PH];

@@ -25,11 +25,11 @@ cudaError_t launch_paged_single(int D, int GP, const Launch& L);
 // the KV head its rows belong to (pages of >= 16 rows, <= 8 columns per KV head, GP == 16).
 cudaError_t launch_paged_multi(int D, int GP, bool warp_head, const Launch& L);
 cudaError_t launch_sparse(int D, int GP, const Launch& L);
-// Sparse units of 33..64 query heads at head dim 128 on the tcgen05 kernel (sparse_tc.cu): block
-// size, selection entries per CTA, launch.
+// Sparse units of 33..64 query heads (head dim 64 or 128) on the tcgen05 kernel (sparse_tc.cu):
+// block size, selection entries per CTA, launch.
 int sparse_tc_threads();
 int sparse_tc_chunk();
-cudaError_t launch_sparse_tc(const Launch& L);
+cudaError_t launch_sparse_tc(int D, const Launch& L);
 
 // One 32-thread block whose bounded wait on a never-completed barrier times out after limit_ns
 // and records kErrWaitCheck in *err.

@@ -1,10 +1,10 @@
 // Sparse decode attention on the fifth-generation tensor cores (tcgen05), for units of 33..64
-// query heads per KV head at head dim 128.
+// query heads per KV head at head dim 64 or 128.
 //
 // Why a second sparse kernel.  With more than 32 query heads per KV head the mma.sync kernel
 // splits the heads into groups of 32, so every selected row is gathered once per group, and its
 // warp-level MMAs bound the per-tile time.  Here one CTA holds all of the unit's heads: the group
-// is a real dense tile (S = Q K^T is 128 x 64 x 128 with the heads zero-padded to 128 rows), so
+// is a real dense tile (S = Q K^T is 128 x 64 x D with the heads zero-padded to 128 rows), so
 // both products run as tcgen05.mma with the accumulators in tensor memory.
 //
 // Work split.  CTA = (unit u = (b, g), chunk of 512 selection entries); the chunk depends on
@@ -14,12 +14,13 @@
 //
 // Inside a CTA (288 threads):
 //   warps 5-8  producers: gather the chunk's selected K and V rows with 16-byte cp.async into a
-//              ring of 4 stages (64 rows of K and of V each, 128-byte swizzle, rows outside
+//              128 KB ring of stages (64 rows of K and of V each: 4 stages at D = 128, 8 at
+//              D = 64; 128-byte swizzle, rows outside
 //              [0, pool_rows) zero-filled); a stage's full barrier completes when every
 //              producer thread's copies for it have landed (cp.async.mbarrier.arrive), so
 //              the producers run ahead as far as the ring allows;
 //   warp 4     allocates 256 TMEM columns; one lane issues S(t) = Q K(t)^T into one of two
-//              64-column S buffers and O += P(t) V(t) into the 128-column O accumulator (after
+//              64-column S buffers and O += P(t) V(t) into the D-column O accumulator (after
 //              acquiring a stage it fences the generic proxy, in which cp.async wrote the rows,
 //              against the async proxy the MMAs read them through);
 //   warps 0-3  softmax: thread h owns query head h (TMEM lane h).  It reads its row of S(t),
@@ -38,14 +39,9 @@
 namespace da {
 namespace {
 
-constexpr int kTcD = 128;
 constexpr int kTcM = 128;                        // MMA rows: the unit's query heads, zero-padded
 constexpr int kTcChunk = 512;                    // selection entries per CTA
-constexpr int kTcStages = 4;
-constexpr int kTcTileBytes = kTileKeys * kTcD * 2;     // one K (or V) tile, two 64-column halves
-constexpr int kTcStageBytes = 2 * kTcTileBytes;
-constexpr int kTcQBytes = kTcM * kTcD * 2;             // [2 halves][128 rows][128 B]
-constexpr int kTcPBytes = kTcM * kTileKeys * 2;        // [128 rows][128 B]: one tile's weights
+constexpr int kTcPBytes = kTcM * kTileKeys * 2;  // [128 rows][128 B]: one tile's bf16 weights
 constexpr int kTcSoftmaxWarps = 4;
 constexpr int kTcMmaWarp = 4;
 constexpr int kTcProducerWarps = 4;
@@ -53,59 +49,79 @@ constexpr int kTcThreads = 32 * (kTcSoftmaxWarps + 1 + kTcProducerWarps);
 constexpr uint32_t kTcCols = 256;                // TMEM: S buffers at columns 0 and 64, O at 128
 constexpr uint32_t kTcColO = 128;
 constexpr float kTcRescaleLog2 = 8.f;
-// tc_merge stages the rows of up to this many segments of 64 heads in the stage ring (4)
-constexpr int kTcMergeSegments = kTcStages * kTcStageBytes / (64 * kTcD * 4);
-constexpr int kTcRowStride = kTcD + 4;           // floats between staged O rows (bank spread)
+constexpr int kTcRingBytes = 128 * 1024;         // the stage ring
+constexpr int kTcMaxStages = 8;
+constexpr int kTcMergeSegments = 4;              // tc_merge stages up to this many segments
 
-// shared-memory layout, from a 1024-byte aligned base
-constexpr int kOffQ = kTcStages * kTcStageBytes;
-constexpr int kOffP = kOffQ + kTcQBytes;
-constexpr int kOffBar = kOffP + 2 * kTcPBytes;
-constexpr int kOffIdx = kOffBar + 1024;
-constexpr int kTcSmemBytes = 1024 + kOffIdx + kTcChunk * 4;
-static_assert(kTcSmemBytes <= kSmemBudget, "shared memory");
+// Head-dim dependent sizes and the shared-memory layout (from a 1024-byte aligned base).
+template <int D>
+struct TcGeom {
+    static_assert(D == 64 || D == 128, "head dim");
+    static constexpr int kHalves = D / 64;                     // 64-column (128-byte) halves
+    static constexpr int kTileBytes = kTileKeys * D * 2;       // one K (or V) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kStages = kTcRingBytes / kStageBytes; // 4 at D 128, 8 at D 64
+    static constexpr int kQBytes = kTcM * D * 2;               // [halves][128 rows][128 B]
+    static constexpr int kD4 = D / 4;                          // float4 columns of a row
+    static constexpr int kHeadsPerInstr = 32 / kD4;            // rows one warp access covers
+    static constexpr int kRowStride = D + 4;                   // floats between staged O rows
+    static constexpr int kOffQ = kTcRingBytes;
+    static constexpr int kOffP = kOffQ + kQBytes;
+    static constexpr int kOffBar = kOffP + 2 * kTcPBytes;
+    static constexpr int kOffIdx = kOffBar + 1024;
+    static constexpr int kSmemBytes = 1024 + kOffIdx + kTcChunk * 4;
+    static_assert(kStages <= kTcMaxStages, "stage ring");
+    static_assert(kSmemBytes <= kSmemBudget, "shared memory");
+    static_assert(64 * kRowStride * 4 <= kTcRingBytes, "staged O rows");
+    static_assert(kTcMergeSegments * 64 * D * 4 <= kTcRingBytes, "merge rows");
+    static_assert((kTcMergeSegments + 3) * 64 * 4 <= kQBytes, "merge weights");
+};
 static_assert(kTcSoftmaxWarps * 32 == kConsumerThreads, "the merge runs on the softmax warps");
-static_assert(64 * kTcRowStride * 4 <= kTcStages * kTcStageBytes, "staged O rows");
-static_assert((kTcMergeSegments + 3) * 64 * 4 <= kTcQBytes, "merge weights");
 
 struct TcBars {
-    uint64_t full[kTcStages];    // stage's K and V rows landed (count: producer threads + 1)
-    uint64_t empty[kTcStages];   // stage's P.V completed (tcgen05.commit)
-    uint64_t s_ready[2];         // S buffer written (tcgen05.commit)
-    uint64_t s_free[2];          // S buffer read by the softmax warps (count: active warps)
-    uint64_t p_ready[2];         // P buffer written, O rescaled (count: active warps)
-    uint64_t pv_done[2];         // P.V of the tile with this parity completed (tcgen05.commit)
-    uint64_t q_ready;            // Q in shared memory (count: softmax threads)
-    uint64_t tmem_done;          // softmax warps finished with TMEM (count: softmax warps)
-    uint64_t drain;              // every MMA issued so far completed (tcgen05.commit)
-    uint64_t group;              // softmax-warp group barrier of the merge
-    uint64_t mrows;              // merge: a batch of partial rows landed (bulk copies)
-    uint64_t stage_mask[kTcStages];
+    uint64_t full[kTcMaxStages];   // stage's K and V rows landed (count: producer threads + 1)
+    uint64_t empty[kTcMaxStages];  // stage's P.V completed (tcgen05.commit)
+    uint64_t s_ready[2];           // S buffer written (tcgen05.commit)
+    uint64_t s_free[2];            // S buffer read by the softmax warps (count: active warps)
+    uint64_t p_ready[2];           // P buffer written, O rescaled (count: active warps)
+    uint64_t pv_done[2];           // P.V of the tile with this parity completed (tcgen05.commit)
+    uint64_t q_ready;              // Q in shared memory (count: softmax threads)
+    uint64_t tmem_done;            // softmax warps finished with TMEM (count: softmax warps)
+    uint64_t drain;                // every MMA issued so far completed (tcgen05.commit)
+    uint64_t group;                // softmax-warp group barrier of the merge
+    uint64_t mrows;                // merge: the partial rows landed (bulk copies)
+    uint64_t stage_mask[kTcMaxStages];
     uint32_t tmem_base;
     int abort;
     int last_flag;
 };
 static_assert(sizeof(TcBars) <= 1024, "barrier block");
 
-// Merges the nseg <= kTcMergeSegments partial rows of a unit of G <= 64 heads (workspace segments
-// first_seg, ...; one segment's rows are G * 512 contiguous bytes) by log-sum-exp in segment order
-// and stores its bf16 output rows; runs on the 128 softmax threads.  The arithmetic is
-// merge_unit's: the maximum over every segment's LSE, weights exp2(lse - max) of the live
-// segments summed in segment order from the first live one, rows accumulated in the same order
-// by fma from zero, the output acc * (1 / sum), and a head with a single live segment copies that
-// segment's row.  All rows land in `rows_sm` (the idle stage ring) by bulk copies that
-// thread 0 issues while the per-head weights are formed in `w_sm`; thread (warp w, lane c) then
-// takes float4 column c of heads w, w + 4, ..., eight heads at a time.  The caller has acquired
-// every segment's rows (the unit's counter) before the call.
+// Merges the nseg <= kTcMergeSegments partial rows of a unit of G <= 64 heads (workspace
+// segments first_seg, ...; one segment's rows are G * D * 4 contiguous bytes) by log-sum-exp in
+// segment order and stores its bf16 output rows; runs on the 128 softmax threads.  The arithmetic
+// is merge_unit's: the maximum over every segment's LSE, weights exp2(lse - max) of the live
+// segments summed in segment order from the first live one, rows accumulated in the same order by
+// fma from zero, the output acc * (1 / sum), and a head with a single live segment copies that
+// segment's row.  All rows land in `rows_sm` (the idle stage ring) by bulk copies that thread 0
+// issues while the per-head weights are formed in `w_sm`; a warp access then covers
+// kHeadsPerInstr heads (lane = one float4 column of one of them), and a thread takes its heads
+// four at a time with every load of a pass in flight.  The caller has acquired every segment's
+// rows (the unit's counter) before the call.
+template <int D>
 __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, float* w_sm,
-                                      unsigned char* rows_sm, uint64_t* mrows, int hq0, int G,
-                                      int first_seg, int nseg, uint32_t& gphase) {
-    constexpr int D4 = kTcD / 4;
-    constexpr int kHeadsPerThread = 64 / kTcSoftmaxWarps;
+                                         unsigned char* rows_sm, uint64_t* mrows, int hq0, int G,
+                                         int first_seg, int nseg, uint32_t& gphase) {
+    using Tg = TcGeom<D>;
+    constexpr int D4 = Tg::kD4;
+    constexpr int R = Tg::kHeadsPerInstr;                    // heads per warp access
+    constexpr int kHeadsPerThread = 64 / (kTcSoftmaxWarps * R);
     constexpr int kPass = 4;                                 // heads per pass and thread
-    const int tid = threadIdx.x, wv = tid >> 5, c = tid & 31;
+    const int tid = threadIdx.x, wv = tid >> 5;
+    const int c = (tid & 31) % D4, sub = (tid & 31) / D4;
+    auto head_of = [&](int j) { return (wv + kTcSoftmaxWarps * j) * R + sub; };
     const size_t SH = static_cast<size_t>(p.seg_heads);
-    const uint32_t seg_bytes = static_cast<uint32_t>(G) * kTcD * 4;
+    const uint32_t seg_bytes = static_cast<uint32_t>(G) * D * 4;
     const float* lse = p.part_lse + static_cast<size_t>(first_seg) * SH;
     const float4* src = reinterpret_cast<const float4*>(p.part_o) + static_cast<size_t>(first_seg) * SH * D4;
     const float4* rs = reinterpret_cast<const float4*>(rows_sm);
@@ -151,16 +167,16 @@ __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, fl
         return false;
     }
     if (!group_sync(sm, gphase, p.err)) return false;   // weights visible
-    // Passes of kPass heads per thread.  Every load of a pass (the heads' statistics and all their
-    // segments' weights and rows) is independent of the others and predicated rather than
-    // branched around, so they are all in flight together.
+    // Every load of a pass (the heads' statistics and all their segments' weights and rows) is
+    // independent of the others and predicated rather than branched around, so they are all in
+    // flight together.
 #pragma unroll 1
     for (int j0 = 0; j0 < kHeadsPerThread; j0 += kPass) {
         int live[kPass], only[kPass];
         float inv[kPass];
 #pragma unroll
         for (int j = 0; j < kPass; ++j) {
-            const int h = min(wv + kTcSoftmaxWarps * (j0 + j), G - 1);
+            const int h = min(head_of(j0 + j), G - 1);
             live[j] = h_live[h];
             only[j] = h_only[h];
             inv[j] = h_inv[h];
@@ -171,7 +187,7 @@ __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, fl
         for (int k = 0; k < kTcMergeSegments; ++k)
 #pragma unroll
             for (int j = 0; j < kPass; ++j) {
-                const int hj = wv + kTcSoftmaxWarps * (j0 + j);
+                const int hj = head_of(j0 + j);
                 const int h = min(hj, G - 1);
                 const int kk = min(k, nseg - 1);
                 w[k][j] = (k < nseg && hj < G) ? w_sm[kk * 64 + h] : 0.f;
@@ -186,27 +202,30 @@ __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, fl
                 const float4 f = fma4(w[k][j], o[k][j], acc);
                 acc = w[k][j] != 0.f ? f : acc;
             }
-            const int h = wv + kTcSoftmaxWarps * (j0 + j);
+            const int h = head_of(j0 + j);
             const float4 single = rs[(only[j] * G + min(h, G - 1)) * D4 + c];
             const float4 scaled = make_float4(acc.x * inv[j], acc.y * inv[j], acc.z * inv[j], acc.w * inv[j]);
             const float4 v = live[j] == 1 ? single : (live[j] > 1 ? scaled : make_float4(0.f, 0.f, 0.f, 0.f));
             if (h < G)
-                *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(hq0 + h) * kTcD + 4 * c) =
+                *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(hq0 + h) * D + 4 * c) =
                     make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
         }
     }
     return true;
 }
 
+template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
                  const Params p) {
+    using Tg = TcGeom<D>;
+    constexpr int S = Tg::kStages;
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte aligned by an offset into the shared array, so accesses through `base` stay
     // shared-memory accesses for the compiler
     unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    TcBars& bar = *reinterpret_cast<TcBars*>(base + kOffBar);
-    int* sidx = reinterpret_cast<int*>(base + kOffIdx);
+    TcBars& bar = *reinterpret_cast<TcBars*>(base + Tg::kOffBar);
+    int* sidx = reinterpret_cast<int*>(base + Tg::kOffIdx);
     volatile int* abort = &bar.abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G;
@@ -221,7 +240,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
     const int hq0 = b * p.Hq + g * G;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTcStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&bar.full[s], 32 * kTcProducerWarps + 1);
             mbar_init(&bar.empty[s], 1);
         }
@@ -262,17 +281,21 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
             sidx[i] = (idx >= 0 && idx < p.pool_rows) ? idx : -1;
         }
         asm volatile("bar.sync 1, %0;" ::"r"(32 * kTcProducerWarps) : "memory");   // producers only
-        // lanes 0-15 copy the 16 chunks of a K row, lanes 16-31 those of the V row
-        const bool isv = lane >= 16;
-        const int c = lane & 15;
+        // a warp instruction copies kRowsPerInstr rows: in each group of 2 * CH lanes the first CH
+        // copy the 16-byte chunks of a K row, the other CH those of the V row
+        constexpr int CH = D / 8;
+        constexpr int kRowsPerInstr = 32 / (2 * CH);
+        const int sub = lane / (2 * CH), w = lane % (2 * CH);
+        const bool isv = w >= CH;
+        const int c = isv ? w - CH : w;
         const __nv_bfloat16* pool = (isv ? p.v_pool : p.k_pool) +
-                                    static_cast<size_t>(u) * p.pool_rows * kTcD + c * 8;
+                                    static_cast<size_t>(u) * p.pool_rows * D + c * 8;
         constexpr int kRowsPerWarp = kTileKeys / kTcProducerWarps;
         bool ok = true;
         int t = 0;
         for (; t < ntiles; ++t) {
-            const int s = t % kTcStages;
-            if (!mbar_wait_warp(&bar.empty[s], ((t / kTcStages) & 1) ^ 1u, abort)) {
+            const int s = t % S;
+            if (!mbar_wait_warp(&bar.empty[s], ((t / S) & 1) ^ 1u, abort)) {
                 ok = false;
                 break;
             }
@@ -285,14 +308,15 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
                                       (static_cast<uint64_t>(__ballot_sync(0xffffffffu, v1)) << 32);
                 if (lane == 0) bar.stage_mask[s] = mask;
             }
-            unsigned char* tile = base + s * kTcStageBytes + (isv ? kTcTileBytes : 0);
+            unsigned char* tile = base + s * Tg::kStageBytes + (isv ? Tg::kTileBytes : 0);
 #pragma unroll 8
-            for (int r = pw * kRowsPerWarp; r < (pw + 1) * kRowsPerWarp; ++r) {
+            for (int rb = pw * kRowsPerWarp; rb < (pw + 1) * kRowsPerWarp; rb += kRowsPerInstr) {
+                const int r = rb + sub;
                 const int li = l0 + r;
                 const int idx = li < nkeys ? sidx[li] : -1;
                 const bool valid = idx >= 0;
-                cp_async_16(tile + tile_offset<2>(r, c, 6),
-                            pool + static_cast<size_t>(valid ? idx : 0) * kTcD, valid ? 16u : 0u);
+                cp_async_16(tile + tile_offset<Tg::kHalves>(r, c, 6),
+                            pool + static_cast<size_t>(valid ? idx : 0) * D, valid ? 16u : 0u);
             }
             cp_async_arrive_noinc(&bar.full[s]);
             if (ptid == 0) mbar_arrive(&bar.full[s]);   // publishes the stage mask
@@ -310,19 +334,19 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
         // ============================================================ MMA warp
         if (lane == 0) {
             constexpr uint32_t kIdS = umma_idesc_bf16(kTcM, kTileKeys, false);
-            constexpr uint32_t kIdO = umma_idesc_bf16(kTcM, kTcD, true);
-            const uint32_t q_s = smem_u32(base + kOffQ);
+            constexpr uint32_t kIdO = umma_idesc_bf16(kTcM, D, true);
+            const uint32_t q_s = smem_u32(base + Tg::kOffQ);
             // S(t) = Q K(t)^T into S buffer t % 2: A = Q (K-major), B = the K tile (K-major)
             auto issue_s = [&](int t) -> bool {
-                const int s = t % kTcStages, sb = t & 1;
-                if (!mbar_wait(&bar.full[s], (t / kTcStages) & 1, abort, kWaitLimitNs)) return false;
+                const int s = t % S, sb = t & 1;
+                if (!mbar_wait(&bar.full[s], (t / S) & 1, abort, kWaitLimitNs)) return false;
                 if (t >= 2 && !mbar_wait(&bar.s_free[sb], ((t - 2) >> 1) & 1, abort, kWaitLimitNs))
                     return false;
                 fence_proxy_async_smem();
                 tc_fence_after_sync();
-                const uint32_t k_s = smem_u32(base + s * kTcStageBytes);
+                const uint32_t k_s = smem_u32(base + s * Tg::kStageBytes);
 #pragma unroll
-                for (int ks = 0; ks < kTcD / 16; ++ks) {
+                for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks & 3) * 32u;   // 16 dims = 32 B into the swizzled row
                     const uint64_t a = umma_desc_sw128(q_s + (ks >> 2) * (kTcM * 128) + off, 16, 1024);
                     const uint64_t bd = umma_desc_sw128(k_s + (ks >> 2) * (kTileKeys * 128) + off, 16, 1024);
@@ -341,15 +365,15 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
                     ok = false;
                     break;
                 }
-                const int s = t % kTcStages, pb = t & 1;
+                const int s = t % S, pb = t & 1;
                 if (!mbar_wait(&bar.p_ready[pb], (t >> 1) & 1, abort, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 // O += P(t) V(t): A = P (K-major), B = the V tile (MN-major: dims contiguous)
-                const uint32_t p_s = smem_u32(base + kOffP + pb * kTcPBytes);
-                const uint32_t v_s = smem_u32(base + s * kTcStageBytes + kTcTileBytes);
+                const uint32_t p_s = smem_u32(base + Tg::kOffP + pb * kTcPBytes);
+                const uint32_t v_s = smem_u32(base + s * Tg::kStageBytes + Tg::kTileBytes);
 #pragma unroll
                 for (int ks = 0; ks < kTileKeys / 16; ++ks) {
                     const uint64_t a = umma_desc_sw128(p_s + ks * 32, 16, 1024);
@@ -382,23 +406,24 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     {
         // Q rows of the unit (zero past G) in the A-operand layout; zero P rows past G
-        unsigned char* qs = base + kOffQ;
-        constexpr int kPer = kTcM * (kTcD / 8) / kConsumerThreads;   // 16-byte chunks per thread
+        unsigned char* qs = base + Tg::kOffQ;
+        constexpr int CQ = D / 8;                                     // 16-byte chunks per row
+        constexpr int kPer = kTcM * CQ / kConsumerThreads;            // 16-byte chunks per thread
         uint4 v[kPer];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-            const int i = threadIdx.x + k * kConsumerThreads, r = i >> 4, c = i & 15;
-            v[k] = r < G ? __ldg(reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(hq0 + r) * kTcD) + c)
+            const int i = threadIdx.x + k * kConsumerThreads, r = i / CQ, c = i % CQ;
+            v[k] = r < G ? __ldg(reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(hq0 + r) * D) + c)
                          : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-            const int i = threadIdx.x + k * kConsumerThreads, r = i >> 4, c = i & 15;
+            const int i = threadIdx.x + k * kConsumerThreads, r = i / CQ, c = i % CQ;
             *reinterpret_cast<uint4*>(qs + (c >> 3) * (kTcM * 128) + r * 128 + (((c ^ r) & 7) << 4)) = v[k];
         }
         if (!live)
             for (int i = 0; i < 2 * (kTileKeys / 8); ++i)
-                *reinterpret_cast<uint4*>(base + kOffP + (i >> 3) * kTcPBytes + h * 128 + (i & 7) * 16) =
+                *reinterpret_cast<uint4*>(base + Tg::kOffP + (i >> 3) * kTcPBytes + h * 128 + (i & 7) * 16) =
                     make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
         mbar_arrive(&bar.q_ready);
@@ -409,8 +434,8 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
     bool ok = true;
     if (warp_active) {
         for (int t = 0; t < ntiles; ++t) {
-            const int s = t % kTcStages, sb = t & 1;
-            if (!mbar_wait_warp(&bar.full[s], (t / kTcStages) & 1, abort) ||
+            const int s = t % S, sb = t & 1;
+            if (!mbar_wait_warp(&bar.full[s], (t / S) & 1, abort) ||
                 !mbar_wait_warp(&bar.s_ready[sb], (t >> 1) & 1, abort)) {
                 ok = false;
                 break;
@@ -451,7 +476,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
                 tc_fence_after_sync();
                 const float a = rescale ? alpha : 1.f;
 #pragma unroll
-                for (int cb = 0; cb < kTcD / 32; ++cb) {
+                for (int cb = 0; cb < D / 32; ++cb) {
                     uint32_t o[32];
                     tmem_ld32(t_lane + kTcColO + cb * 32, o);
                     tmem_wait_ld();
@@ -481,7 +506,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
                 ok = false;
                 break;
             }
-            unsigned char* prow = base + kOffP + sb * kTcPBytes + h * 128;
+            unsigned char* prow = base + Tg::kOffP + sb * kTcPBytes + h * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 *reinterpret_cast<uint4*>(prow + (((c ^ h) & 7) << 4)) =
@@ -496,7 +521,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
     }
 
     // The normalised O rows go through shared memory (row h of the idle stage ring,
-    // kTcRowStride floats apart) so that the global stores are coalesced: the output rows (one
+    // Tg::kRowStride floats apart) so that the global stores are coalesced: the output rows (one
     // chunk) or this chunk's partial rows and LSEs.
     const bool whole = p.nchunks == 1;
     const size_t SH = static_cast<size_t>(p.seg_heads);
@@ -506,7 +531,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
         const bool empty = !(l_run > 0.f);
         const float inv = empty ? 0.f : 1.0f / l_run;
 #pragma unroll
-        for (int cb = 0; cb < kTcD / 32; cb += 2) {
+        for (int cb = 0; cb < D / 32; cb += 2) {
             // two 32-column loads in flight per wait
             uint32_t o[2][32];
             tmem_ld32(t_lane + kTcColO + cb * 32, o[0]);
@@ -515,7 +540,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
             if (!live) continue;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                float4* dst = reinterpret_cast<float4*>(orow_sm + h * kTcRowStride + (cb + half) * 32);
+                float4* dst = reinterpret_cast<float4*>(orow_sm + h * Tg::kRowStride + (cb + half) * 32);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     dst[j] = make_float4(__uint_as_float(o[half][4 * j]) * inv,
@@ -544,23 +569,25 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
     uint32_t gphase = 0;
     if (!group_sync(sm, gphase, p.err)) return;   // rows staged
     {
-        // thread (warp w, lane c): float4 column c of heads w, w + 4, ...; a fixed trip count, so
-        // all sixteen shared-memory loads are in flight before the stores
-        const int wv = warp, c = lane;
-        constexpr int kPer = 64 / kTcSoftmaxWarps;
+        // a warp access covers kHeadsPerInstr heads, lane = one float4 column of one of them; a
+        // fixed trip count, so all of a thread's shared-memory loads are in flight before the stores
+        constexpr int D4 = Tg::kD4, R = Tg::kHeadsPerInstr;
+        constexpr int kPer = 64 / (kTcSoftmaxWarps * R);
+        const int c = lane % D4, sub = lane / D4;
         float4 v[kPer];
 #pragma unroll
         for (int j = 0; j < kPer; ++j)
-            v[j] = *reinterpret_cast<const float4*>(orow_sm + min(wv + kTcSoftmaxWarps * j, G - 1) * kTcRowStride + 4 * c);
+            v[j] = *reinterpret_cast<const float4*>(
+                orow_sm + min((warp + kTcSoftmaxWarps * j) * R + sub, G - 1) * Tg::kRowStride + 4 * c);
 #pragma unroll
         for (int j = 0; j < kPer; ++j) {
-            const int hh = wv + kTcSoftmaxWarps * j;
+            const int hh = (warp + kTcSoftmaxWarps * j) * R + sub;
             if (hh >= G) continue;
             if (whole)
-                *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(hq0 + hh) * kTcD + 4 * c) =
+                *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(hq0 + hh) * D + 4 * c) =
                     make_uint2(pack_bf16x2(v[j].x, v[j].y), pack_bf16x2(v[j].z, v[j].w));
             else
-                *reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(blockIdx.x) * SH + hh) * kTcD + 4 * c) = v[j];
+                *reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(blockIdx.x) * SH + hh) * D + 4 * c) = v[j];
         }
     }
     if (whole) return;
@@ -585,9 +612,9 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
         // the Q area holds the merge's per-segment weights and the stage ring its rows; more
         // chunks take the general merge (same arithmetic; the stage ring is its scratch)
         const bool ok_m = p.nchunks <= kTcMergeSegments
-                              ? tc_merge(p, sm, reinterpret_cast<float*>(base + kOffQ), base, &bar.mrows,
-                                         hq0, G, u * p.nchunks, p.nchunks, gphase)
-                              : merge_unit<kTcD, 64>(p, sm, U, u * p.nchunks, p.nchunks, gphase);
+                              ? tc_merge<D>(p, sm, reinterpret_cast<float*>(base + Tg::kOffQ), base,
+                                            &bar.mrows, hq0, G, u * p.nchunks, p.nchunks, gphase)
+                              : merge_unit<D, 64, true>(p, sm, U, u * p.nchunks, p.nchunks, gphase);
         if (!ok_m) return;
         if (threadIdx.x == 0) p.counters[u] = 0u;
     }
@@ -599,8 +626,14 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
 int sparse_tc_threads() { return kTcThreads; }
 int sparse_tc_chunk() { return kTcChunk; }
 
-cudaError_t launch_sparse_tc(const Launch& L) {
-    return launch_kernel(reinterpret_cast<const void*>(&sparse_tc_kernel), kTcSmemBytes, L);
+cudaError_t launch_sparse_tc(int D, const Launch& L) {
+    if (D == 128)
+        return launch_kernel(reinterpret_cast<const void*>(&sparse_tc_kernel<128>),
+                             TcGeom<128>::kSmemBytes, L);
+    if (D == 64)
+        return launch_kernel(reinterpret_cast<const void*>(&sparse_tc_kernel<64>),
+                             TcGeom<64>::kSmemBytes, L);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace da
