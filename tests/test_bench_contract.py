@@ -57,3 +57,13 @@ def test_kernel_kind_follows_the_library_dispatch():
     assert any("sparse_tc.cu" in f for f in bench.KERNEL_SOURCES["sparse_tc"])
     assert bench.kernel_label(W.CONFIGS["sparse_selected"]) == "sparse_tc_kernel"
     assert len({bench.kernel_sha(k) for k in bench.KERNEL_SOURCES}) == 3
+
+
+def test_committed_traffic_records_match_the_kernel_sources():
+    """profiles/dram_traffic.json holds, for every named workload but the launch-bound tiny one,
+    the DRAM bytes of an ncu capture of the kernel code as it stands (bench.py reports a record
+    as roofline.traffic only while the hash of the timed kernel's sources agrees)."""
+    import bench
+    from token_decode_attention_split_gb300 import workloads as W
+    stale = [n for n in W.CONFIGS if n != "dense_tiny" and bench.traffic_record(n) is None]
+    assert not stale, f"recapture the profiles of {stale}"

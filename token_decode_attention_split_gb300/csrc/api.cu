@@ -177,27 +177,16 @@ int persistent_ctas(int dev) {
     return (lim > 0 && lim < sms) ? lim : sms;
 }
 
-// Sparse work split.  33..64 query heads per KV head run on the tensor-core kernel: one CTA per
-// (unit, chunk of 512 entries) with all of the unit's heads.  Otherwise the mma.sync kernel:
-// chunks of 512 entries for the (at most 32) heads of a unit.  Both depend on G and D only,
-// never on the width, B or the device.
+// Sparse work split: one CTA per (sequence and KV head, chunk of 512 selection entries) with all
+// of the unit's G <= 64 query heads.  33..64 heads run on the tensor-core kernel, up to 32 on the
+// mma.sync kernel (which holds at most 32 query columns).  The chunk depends on nothing, not on
+// the width, B or the device, so trailing pads never move a chunk boundary.
 bool sparse_uses_tc(int G, int D) {
     return (D == 64 || D == 128) && G > kSparseHeadGroup && G <= 64;
 }
-int sparse_head_groups(int G, int D) {
-    if (sparse_uses_tc(G, D) || G <= kSparseHeadGroup) return 1;
-    return (G + kSparseHeadGroup - 1) / kSparseHeadGroup;
-}
-int sparse_segment_heads(int G, int D) {
-    return (sparse_uses_tc(G, D) || G <= kSparseHeadGroup) ? G : kSparseHeadGroup;
-}
 int sparse_padded_group(int G) { return G <= 8 ? 8 : G <= 16 ? 16 : 32; }
-long long sparse_chunk_keys(int G, int D) {
-    if (sparse_uses_tc(G, D)) return sparse_tc_chunk();
-    return static_cast<long long>(kSparseChunkUnit) * sparse_head_groups(G, D);
-}
-long long sparse_chunks(long long width, int G, int D) {
-    return (width + sparse_chunk_keys(G, D) - 1) / sparse_chunk_keys(G, D);
+long long sparse_chunks(long long width) {
+    return (width + kSparseChunkUnit - 1) / kSparseChunkUnit;
 }
 
 }  // namespace
@@ -276,8 +265,7 @@ size_t decode_attn_workspace_size(int variant, int B, int Hq, int Hkv, int D, in
         segments = units + sms;
     } else if (variant == DA_VARIANT_SPARSE) {
         if (max_kv < 0) return 0;
-        const long long groups = units * sparse_head_groups(G, D);
-        return ws_layout(groups, groups * sparse_chunks(max_kv, G, D), sparse_segment_heads(G, D), D).total;
+        return ws_layout(units, units * sparse_chunks(max_kv), G, D).total;
     } else {
         return 0;
     }
@@ -544,15 +532,14 @@ da_status decode_attn_sparse(const void* q, const void* k_pool, const void* v_po
     if (pool_rows >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
     const long long units = static_cast<long long>(B) * Hkv;
     const int G = Hq / Hkv;
-    const long long groups = units * sparse_head_groups(G, D);
-    const long long chunks = sparse_chunks(width, G, D);
-    if (groups * chunks >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
+    const long long chunks = sparse_chunks(width);
+    if (units * chunks >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (B == 0) return DA_OK;
     const int dev = current_device();
     if (dev < 0) return DA_ERR_CUDA;
     const int GP = sparse_padded_group(G);
-    const WsLayout w = ws_layout(groups, groups * chunks, sparse_segment_heads(G, D), D);
+    const WsLayout w = ws_layout(units, units * chunks, G, D);
     if (workspace_bytes < w.total) return DA_ERR_WORKSPACE_TOO_SMALL;
     if (width == 0) return zero_output(out, B, Hq, D, cs);
 
@@ -563,12 +550,12 @@ da_status decode_attn_sparse(const void* q, const void* k_pool, const void* v_po
     L.p.width = width;
     L.p.pool_rows = static_cast<int>(pool_rows);
     L.p.nchunks = static_cast<int>(chunks);
-    L.p.nhg = sparse_head_groups(G, D);
-    L.p.chunk_keys = static_cast<int>(sparse_chunk_keys(G, D));
-    L.p.seg_heads = sparse_segment_heads(G, D);
+    L.p.nhg = 1;
+    L.p.chunk_keys = kSparseChunkUnit;
+    L.p.seg_heads = G;
     L.p.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
     L.p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
-    L.grid = static_cast<int>(groups * chunks);
+    L.grid = static_cast<int>(units * chunks);
     L.stream = cs;
     if (sparse_uses_tc(G, D)) {
         L.threads = sparse_tc_threads();

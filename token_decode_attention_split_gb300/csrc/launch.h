@@ -26,9 +26,8 @@ cudaError_t launch_paged_single(int D, int GP, const Launch& L);
 cudaError_t launch_paged_multi(int D, int GP, bool warp_head, const Launch& L);
 cudaError_t launch_sparse(int D, int GP, const Launch& L);
 // Sparse units of 33..64 query heads (head dim 64 or 128) on the tcgen05 kernel (sparse_tc.cu):
-// block size, selection entries per CTA, launch.
+// block size and launch; its chunks are kSparseChunkUnit entries like the mma.sync kernel's.
 int sparse_tc_threads();
-int sparse_tc_chunk();
 cudaError_t launch_sparse_tc(int D, const Launch& L);
 
 // One 32-thread block whose bounded wait on a never-completed barrier times out after limit_ns

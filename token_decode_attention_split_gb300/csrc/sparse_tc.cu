@@ -40,7 +40,7 @@ namespace da {
 namespace {
 
 constexpr int kTcM = 128;                        // MMA rows: the unit's query heads, zero-padded
-constexpr int kTcChunk = 512;                    // selection entries per CTA
+constexpr int kTcChunk = kSparseChunkUnit;       // selection entries per CTA (512)
 constexpr int kTcPBytes = kTcM * kTileKeys * 2;  // [128 rows][128 B]: one tile's bf16 weights
 constexpr int kTcSoftmaxWarps = 4;
 constexpr int kTcMmaWarp = 4;
@@ -624,7 +624,6 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
 }  // namespace
 
 int sparse_tc_threads() { return kTcThreads; }
-int sparse_tc_chunk() { return kTcChunk; }
 
 cudaError_t launch_sparse_tc(int D, const Launch& L) {
     if (D == 128)
