@@ -182,7 +182,7 @@ int persistent_ctas(int dev) {
 // mma.sync kernel (which holds at most 32 query columns).  The chunk depends on nothing, not on
 // the width, B or the device, so trailing pads never move a chunk boundary.
 bool sparse_uses_tc(int G, int D) {
-    return (D == 64 || D == 128) && G > kSparseHeadGroup && G <= 64;
+    return (D == 64 || D == 128) && G > kSparseMaxHeads && G <= 64;
 }
 int sparse_padded_group(int G) { return G <= 8 ? 8 : G <= 16 ? 16 : 32; }
 long long sparse_chunks(long long width) {
@@ -550,8 +550,6 @@ da_status decode_attn_sparse(const void* q, const void* k_pool, const void* v_po
     L.p.width = width;
     L.p.pool_rows = static_cast<int>(pool_rows);
     L.p.nchunks = static_cast<int>(chunks);
-    L.p.nhg = 1;
-    L.p.chunk_keys = kSparseChunkUnit;
     L.p.seg_heads = G;
     L.p.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
     L.p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);

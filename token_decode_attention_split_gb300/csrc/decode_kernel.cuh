@@ -8,9 +8,10 @@
 // column then only sees its own KV head's rows.  A unit's live rows are cut into 64-row tiles.
 // Dense and paged calls run a persistent grid (one CTA per SM): the tiles of all units are laid
 // end to end and CTA c takes the contiguous range [c*N/C, (c+1)*N/C), so the load is balanced to
-// one tile whatever the lengths.  Sparse calls give each CTA up to 32 query heads of one unit
-// over one chunk of 512 * ceil(G / 32) selection entries: the chunk depends on G only, so
-// trailing -1 pads cannot move a chunk boundary.  Each CTA's piece of a unit is a "segment".
+// one tile whatever the lengths.  Sparse calls (up to 32 query heads per KV head; larger groups
+// run on the tensor-core kernel) give each CTA one unit over one chunk of 512 selection entries:
+// the chunk is fixed, so trailing -1 pads cannot move a chunk boundary.  Each CTA's piece of a
+// unit is a "segment".
 //
 // Inside a CTA.  The producer warps (one for dense, two taking alternate tiles for paged, four
 // sharing every tile for sparse) stream K and V tiles into a ring of shared-memory stages (TMA
@@ -65,8 +66,8 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, kWaitLimitNs));
 }
-constexpr int kSparseHeadGroup = 32;         // query heads per CTA when a group is split
-constexpr int kSparseChunkUnit = 512;         // sparse chunk = 512 entries per head group
+constexpr int kSparseMaxHeads = 32;          // query heads per KV head of this kernel's sparse units
+constexpr int kSparseChunkUnit = 512;         // sparse chunk: selection entries per CTA
 constexpr int kMaxPagedBatch = 1024;
 constexpr int kSmemBudget = 232448;           // opt-in dynamic shared memory per block
 
@@ -128,8 +129,6 @@ struct Params {
     // sparse
     const int* sel;
     int width, pool_rows, nchunks;
-    int nhg;                  // head groups per KV head (sparse)
-    int chunk_keys;           // selection entries per chunk (sparse), a multiple of 64
     const __nv_bfloat16* k_pool;
     const __nv_bfloat16* v_pool;
 };
@@ -141,7 +140,7 @@ struct Unit {
     int base;   // global index of the unit's first tile
     int hq0;    // q / out row of the first query head this CTA handles
     int nh;     // query heads this CTA handles
-    int cu;     // merge counter of this (unit, head group)
+    int cu;     // merge counter of this unit
 };
 
 struct SmemPtrs {
@@ -894,15 +893,13 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         t0 = static_cast<int>(static_cast<long long>(blockIdx.x) * N / C);
         t1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * N / C);
     }
-    // sparse: this CTA's chunk of one (unit, head group); blockIdx.x = (u * nhg + hg) * nchunks + chunk
-    int sp_u = 0, sp_cu = 0, sp_hg = 0, sp_key0 = 0, sp_nkeys = 0;
+    // sparse: this CTA's chunk of one unit; blockIdx.x = u * nchunks + chunk
+    int sp_u = 0, sp_key0 = 0, sp_nkeys = 0;
     if (VAR == kSparse) {
-        sp_cu = blockIdx.x / p.nchunks;
-        const int chunk = blockIdx.x - sp_cu * p.nchunks;
-        sp_u = sp_cu / p.nhg;
-        sp_hg = sp_cu - sp_u * p.nhg;
-        sp_key0 = chunk * p.chunk_keys;
-        sp_nkeys = min(p.chunk_keys, p.width - sp_key0);
+        sp_u = blockIdx.x / p.nchunks;
+        const int chunk = blockIdx.x - sp_u * p.nchunks;
+        sp_key0 = chunk * kSparseChunkUnit;
+        sp_nkeys = min(kSparseChunkUnit, p.width - sp_key0);
         t0 = sp_key0 / kTileKeys;
         t1 = (sp_key0 + sp_nkeys + kTileKeys - 1) / kTileKeys;
     }
@@ -1125,10 +1122,9 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         U.len = p.width;
         U.nt = 0;
         U.base = 0;
-        const int hgs = p.nhg > 1 ? kSparseHeadGroup : p.G;
-        U.hq0 = U.b * p.Hq + U.g * p.G + sp_hg * hgs;
-        U.nh = min(hgs, p.G - sp_hg * hgs);
-        U.cu = sp_cu;
+        U.hq0 = U.b * p.Hq + U.g * p.G;
+        U.nh = p.G;
+        U.cu = sp_u;
         cs.load_q(p, U.hq0, U.nh);
         cs.reset();
         for (int t = t0; t < t1; ++t, ++it) {
@@ -1145,7 +1141,7 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty + s);
         }
-        finish_segment<D, GP>(p, sm, cs, U, p.nchunks == 1, blockIdx.x, sp_cu * p.nchunks,
+        finish_segment<D, GP>(p, sm, cs, U, p.nchunks == 1, blockIdx.x, sp_u * p.nchunks,
                               p.nchunks, gphase);
         return;
     }
