@@ -110,7 +110,7 @@ struct Params {
     unsigned* counters;       // one per merge unit, zero between calls
     float* part_o;            // [segments, seg_heads, D]
     float* part_lse;          // [segments, seg_heads] (log2 domain)
-    int seg_heads;            // heads per segment: G, or the head-group size for sparse
+    int seg_heads;            // partial rows per segment: the unit's query columns (kh * G * sq)
     unsigned* err;            // device error word
     // dense
     int k_len;

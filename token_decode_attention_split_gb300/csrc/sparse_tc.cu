@@ -1,11 +1,11 @@
 // Sparse decode attention on the fifth-generation tensor cores (tcgen05), for units of 33..64
 // query heads per KV head at head dim 64 or 128.
 //
-// Why a second sparse kernel.  With more than 32 query heads per KV head the mma.sync kernel
-// splits the heads into groups of 32, so every selected row is gathered once per group, and its
-// warp-level MMAs bound the per-tile time.  Here one CTA holds all of the unit's heads: the group
-// is a real dense tile (S = Q K^T is 128 x 64 x D with the heads zero-padded to 128 rows), so
-// both products run as tcgen05.mma with the accumulators in tensor memory.
+// Why a second sparse kernel.  The mma.sync kernel holds at most 32 query columns, so a larger
+// group would be split into groups of 32 with every selected row gathered once per group, and
+// its warp-level MMAs bound the per-tile time.  Here one CTA holds all of the unit's heads: the
+// group is a real dense tile (S = Q K^T is 128 x 64 x D with the heads zero-padded to 128
+// rows), so both products run as tcgen05.mma with the accumulators in tensor memory.
 //
 // Work split.  CTA = (unit u = (b, g), chunk of 512 selection entries); the chunk depends on
 // nothing but the kernel, so trailing -1 pads cannot move a chunk boundary.  Chunk pieces are
