@@ -123,7 +123,8 @@ __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, fl
     const size_t SH = static_cast<size_t>(p.seg_heads);
     const uint32_t seg_bytes = static_cast<uint32_t>(G) * D * 4;
     const float* lse = p.part_lse + static_cast<size_t>(first_seg) * SH;
-    const float4* src = reinterpret_cast<const float4*>(p.part_o) + static_cast<size_t>(first_seg) * SH * D4;
+    const float4* src =
+        reinterpret_cast<const float4*>(p.part_o) + static_cast<size_t>(first_seg) * SH * D4;
     const float4* rs = reinterpret_cast<const float4*>(rows_sm);
     float* h_inv = w_sm + kTcMergeSegments * 64;             // [64]
     int* h_live = reinterpret_cast<int*>(h_inv + 64);        // [64]
@@ -132,7 +133,8 @@ __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, fl
         fence_proxy_async_global();
         mbar_arrive_expect_tx(mrows, nseg * seg_bytes);
         for (int k = 0; k < nseg; ++k)
-            bulk_load(rows_sm + k * seg_bytes, src + static_cast<size_t>(k) * SH * D4, seg_bytes, mrows);
+            bulk_load(rows_sm + k * seg_bytes, src + static_cast<size_t>(k) * SH * D4, seg_bytes,
+                      mrows);
     }
     if (tid < G) {
         float l[kTcMergeSegments];
@@ -204,8 +206,10 @@ __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, fl
             }
             const int h = head_of(j0 + j);
             const float4 single = rs[(only[j] * G + min(h, G - 1)) * D4 + c];
-            const float4 scaled = make_float4(acc.x * inv[j], acc.y * inv[j], acc.z * inv[j], acc.w * inv[j]);
-            const float4 v = live[j] == 1 ? single : (live[j] > 1 ? scaled : make_float4(0.f, 0.f, 0.f, 0.f));
+            const float4 scaled =
+                make_float4(acc.x * inv[j], acc.y * inv[j], acc.z * inv[j], acc.w * inv[j]);
+            const float4 v =
+                live[j] == 1 ? single : (live[j] > 1 ? scaled : make_float4(0.f, 0.f, 0.f, 0.f));
             if (h < G)
                 *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(hq0 + h) * D + 4 * c) =
                     make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
@@ -348,8 +352,10 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t off = (ks & 3) * 32u;   // 16 dims = 32 B into the swizzled row
-                    const uint64_t a = umma_desc_sw128(q_s + (ks >> 2) * (kTcM * 128) + off, 16, 1024);
-                    const uint64_t bd = umma_desc_sw128(k_s + (ks >> 2) * (kTileKeys * 128) + off, 16, 1024);
+                    const uint64_t a =
+                        umma_desc_sw128(q_s + (ks >> 2) * (kTcM * 128) + off, 16, 1024);
+                    const uint64_t bd =
+                        umma_desc_sw128(k_s + (ks >> 2) * (kTileKeys * 128) + off, 16, 1024);
                     umma_bf16(tmem + sb * kTileKeys, a, bd, kIdS, ks > 0 ? 1u : 0u);
                 }
                 umma_commit(&bar.s_ready[sb]);
@@ -391,7 +397,8 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
             // before the columns are freed
             umma_commit(&bar.drain);
             if (!mbar_wait(&bar.drain, 0, nullptr, kWaitLimitNs)) record_error(p.err, kErrDrain);
-            if (!mbar_wait(&bar.tmem_done, 0, nullptr, kWaitLimitNs)) record_error(p.err, kErrDrain);
+            if (!mbar_wait(&bar.tmem_done, 0, nullptr, kWaitLimitNs))
+                record_error(p.err, kErrDrain);
         }
         __syncwarp();
         tc_fence_after_sync();
@@ -413,18 +420,20 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
             const int i = threadIdx.x + k * kConsumerThreads, r = i / CQ, c = i % CQ;
-            v[k] = r < G ? __ldg(reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(hq0 + r) * D) + c)
+            v[k] = r < G ? __ldg(reinterpret_cast<const uint4*>(p.q +
+                                 static_cast<size_t>(hq0 + r) * D) + c)
                          : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
             const int i = threadIdx.x + k * kConsumerThreads, r = i / CQ, c = i % CQ;
-            *reinterpret_cast<uint4*>(qs + (c >> 3) * (kTcM * 128) + r * 128 + (((c ^ r) & 7) << 4)) = v[k];
+            *reinterpret_cast<uint4*>(qs + (c >> 3) * (kTcM * 128) + r * 128 +
+                                      (((c ^ r) & 7) << 4)) = v[k];
         }
         if (!live)
             for (int i = 0; i < 2 * (kTileKeys / 8); ++i)
-                *reinterpret_cast<uint4*>(base + Tg::kOffP + (i >> 3) * kTcPBytes + h * 128 + (i & 7) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(base + Tg::kOffP + (i >> 3) * kTcPBytes + h * 128 +
+                                          (i & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
         mbar_arrive(&bar.q_ready);
     }
@@ -540,7 +549,8 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
             if (!live) continue;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                float4* dst = reinterpret_cast<float4*>(orow_sm + h * Tg::kRowStride + (cb + half) * 32);
+                float4* dst =
+                    reinterpret_cast<float4*>(orow_sm + h * Tg::kRowStride + (cb + half) * 32);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     dst[j] = make_float4(__uint_as_float(o[half][4 * j]) * inv,
@@ -570,7 +580,8 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
     if (!group_sync(sm, gphase, p.err)) return;   // rows staged
     {
         // a warp access covers kHeadsPerInstr heads, lane = one float4 column of one of them; a
-        // fixed trip count, so all of a thread's shared-memory loads are in flight before the stores
+        // fixed trip count, so all of a thread's shared-memory loads are in flight before the
+        // stores
         constexpr int D4 = Tg::kD4, R = Tg::kHeadsPerInstr;
         constexpr int kPer = 64 / (kTcSoftmaxWarps * R);
         const int c = lane % D4, sub = lane / D4;
@@ -578,7 +589,8 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
 #pragma unroll
         for (int j = 0; j < kPer; ++j)
             v[j] = *reinterpret_cast<const float4*>(
-                orow_sm + min((warp + kTcSoftmaxWarps * j) * R + sub, G - 1) * Tg::kRowStride + 4 * c);
+                orow_sm + min((warp + kTcSoftmaxWarps * j) * R + sub, G - 1) * Tg::kRowStride +
+                4 * c);
 #pragma unroll
         for (int j = 0; j < kPer; ++j) {
             const int hh = (warp + kTcSoftmaxWarps * j) * R + sub;
@@ -587,7 +599,8 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
                 *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(hq0 + hh) * D + 4 * c) =
                     make_uint2(pack_bf16x2(v[j].x, v[j].y), pack_bf16x2(v[j].z, v[j].w));
             else
-                *reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(blockIdx.x) * SH + hh) * D + 4 * c) = v[j];
+                *reinterpret_cast<float4*>(p.part_o +
+                    (static_cast<size_t>(blockIdx.x) * SH + hh) * D + 4 * c) = v[j];
         }
     }
     if (whole) return;
