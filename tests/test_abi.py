@@ -205,3 +205,22 @@ def test_binding_spec_gate_without_gpu(lib):
         assert binding.decode_attn_spec_check(S(softmax_scale=0.125, **{field: 1})) == UNSUPPORTED
     assert binding.decode_attn_spec_check(S(softmax_scale=math.inf)) == INVALID
     assert binding.decode_attn_status_string(UNSUPPORTED)
+
+
+def test_sparse_workspace_size_formula(lib):
+    """Sparse calls need no device to size their workspace: one u32 counter per unit (B * Hkv),
+    then the LSEs and the fp32 partial rows of units * ceil(width / 512) segments of G heads
+    (the chunk of 512 selection entries is the same for both sparse kernels and depends on
+    nothing else), each region starting on a 256-byte boundary."""
+    def expect(B, Hq, Hkv, D, width):
+        G, units = Hq // Hkv, B * Hkv
+        segs = units * -(-width // 512)
+        up = lambda x: -(-x // 256) * 256
+        lse = up(units * 4)
+        o = lse + up(segs * G * 4)
+        return max(o + segs * G * D * 4, 256)
+    for B, Hq, Hkv, D, width in [(32, 64, 1, 128, 2048),   # the sparse workload: 4 MB of rows
+                                 (3, 48, 1, 64, 700), (2, 16, 2, 128, 1), (5, 8, 8, 64, 513),
+                                 (1, 64, 2, 128, 0)]:
+        assert lib.decode_attn_workspace_size(2, B, Hq, Hkv, D, width) == expect(B, Hq, Hkv, D, width)
+    assert lib.decode_attn_workspace_size(2, 32, 64, 1, 128, 2048) > 4 * 2 ** 20
