@@ -15,10 +15,9 @@
 // Inside a CTA (288 threads):
 //   warps 5-8  producers: gather the chunk's selected K and V rows with 16-byte cp.async into a
 //              128 KB ring of stages (64 rows of K and of V each: 4 stages at D = 128, 8 at
-//              D = 64; 128-byte swizzle, rows outside
-//              [0, pool_rows) zero-filled); a stage's full barrier completes when every
-//              producer thread's copies for it have landed (cp.async.mbarrier.arrive), so
-//              the producers run ahead as far as the ring allows;
+//              D = 64; 128-byte swizzle; rows outside [0, pool_rows) zero-filled); a stage's
+//              full barrier completes when every producer thread's copies for it have landed
+//              (cp.async.mbarrier.arrive), so the producers run ahead as far as the ring allows;
 //   warp 4     allocates 256 TMEM columns; one lane issues S(t) = Q K(t)^T into one of two
 //              64-column S buffers and O += P(t) V(t) into the D-column O accumulator (after
 //              acquiring a stage it fences the generic proxy, in which cp.async wrote the rows,
@@ -26,7 +25,10 @@
 //   warps 0-3  softmax: thread h owns query head h (TMEM lane h).  It reads its row of S(t),
 //              masks invalid rows, updates the running maximum and sum, writes its bf16 weights
 //              P(t) into a shared-memory P buffer (the A operand of the second MMA) and, at the
-//              end, normalises its O row and stores it (or its partial and log-sum-exp).
+//              end, normalises its O row; the rows go through shared memory so the stores of
+//              the output (one chunk) or of the partial rows and log-sum-exps are coalesced.
+//              The last CTA of a unit merges: up to four chunks from shared memory, filled by
+//              bulk copies (tc_merge), more with merge_unit, in the same arithmetic.
 // The running maximum used for the weights only moves when a tile's maximum exceeds it by more
 // than 8 (log2 units); the O row is rescaled in TMEM then.  Weights are therefore at most 2^8
 // before bf16 rounding, and the result is the same softmax with a different reference point.
