@@ -1,14 +1,19 @@
 """Decode-attention benchmark: achieved HBM GB/s (and % of the measured GB300 copy peak) and
-µs per call, on one of the named synthetic workloads.
+µs per call, on one of the named synthetic workloads (default: paged_ragged, the largest).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+                    [--min-seconds S]
 
 A step is one decode-attention call over the whole workload (one kernel launch; inputs resident
-in HBM).  The live K/V bytes of every workload but the small ones exceed L2, and two
-independent input copies are alternated between steps, so no step reads what the previous one
-left in L2.  With N > 1 (torchrun), every rank runs its own replica of the workload with its
-own seed; the job value is the bytes of all ranks over the slowest rank's time.
-``--impl reference`` times the fp64 CPU oracle on the host cores instead (a bounded sample).
+in HBM).  K steps are captured in one CUDA graph; after W warm-up steps and about a second of
+untimed replays (steady clocks), the graph is replayed R times between two CUDA events on the
+launching stream, R chosen so the timed region lasts about S seconds (default 4), and the line
+reports the mean per call.  Several independent input copies (same lengths and selections,
+different values) are alternated call by call, as many as it takes for their live bytes to exceed
+the L2 three times over, so no call reads what the previous ones left in L2.  With N > 1
+(torchrun), every rank runs its own replica of the workload with its own seed; the job value is
+the bytes of all ranks over the slowest rank's time.  ``--impl reference`` times the fp64 CPU
+oracle on the host cores instead (a bounded sample of the same workload).
 """
 from __future__ import annotations
 
@@ -32,7 +37,9 @@ from token_decode_attention_split_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and µs per call"
 NOMINAL_HBM_GBS = 8000.0     # the ~8 TB/s nominal HBM3e figure of a GB300, context only
-DEFAULT_WORKLOAD = "dense_batched"
+DEFAULT_WORKLOAD = "paged_ragged"
+L2_BYTES = 129 * 10**6       # GB300 L2 (bytes)
+COPY_BUDGET_BYTES = 48 * 10**9   # device memory the alternated input copies may take
 KERNEL_SOURCES = {
     "decode": ["token_decode_attention_split_gb300/csrc/decode_kernel.cuh",
                "token_decode_attention_split_gb300/csrc/ptx.cuh"],
@@ -192,10 +199,38 @@ class ClockSampler:
 OVERRIDES = {}
 
 
-def make_case(name: str, device, seed_offset: int = 0):
+def make_case(name: str, device, rank: int = 0, copy: int = 0):
+    """Input copy `copy` of rank `rank`'s replica: every copy of a rank shares the integer
+    structure (lengths, pages, selection: the seed) and draws its own values (the value seed)."""
     cfg = dict(W.CONFIGS[name])
     cfg.update(OVERRIDES)
-    return W.make(name, device=device, **{**OVERRIDES, "seed": cfg["seed"] + seed_offset})
+    seed = cfg["seed"] + 1000 * rank
+    return W.make(name, device=device, **{**OVERRIDES, "seed": seed, "value_seed": seed + 100 * copy})
+
+
+def case_device_bytes(case) -> int:
+    """Bytes of every tensor of a case (what one input copy holds on the device)."""
+    n = 0
+    for v in vars(case).values():
+        if isinstance(v, torch.Tensor):
+            n += v.numel() * v.element_size()
+    return n
+
+
+def copies_for(alg: int, device_bytes: int) -> int:
+    """Input copies to alternate: enough that their live bytes exceed the L2 three times over
+    (2 at least, 16 at most), within COPY_BUDGET_BYTES of device memory."""
+    want = max(2, min(16, -(-3 * L2_BYTES // max(1, alg))))
+    fit = max(2, COPY_BUDGET_BYTES // max(1, device_bytes))
+    return int(min(want, fit))
+
+
+def input_copies(case) -> int:
+    return copies_for(case.algorithmic_bytes(), case_device_bytes(case))
+
+
+def l2_note(case) -> str:
+    return l2_note_bytes(case.algorithmic_bytes(), case_device_bytes(case))
 
 
 def parse_overrides(items):
@@ -258,8 +293,10 @@ class HostCopy:
             self.sel = c.sel.cpu().pin_memory()
         self.out = torch.empty(c.out_shape(), dtype=torch.bfloat16).pin_memory()
 
-    def h2d(self, stream):
-        c = self.case
+    def h2d(self, stream, dst=None):
+        """Copies the pinned inputs into `dst` (a case of the same shapes; default: the source
+        case's own device buffers)."""
+        c = self.case if dst is None else dst
         s = stream.cuda_stream
         if c.kind == "append":
             c.k_new.copy_(self.kn, non_blocking=True)
@@ -416,64 +453,81 @@ def cpu_baseline(name: str, budget_s: float = 15.0):
 
 
 def workload_config(name: str, **extra):
-    """The line's `config`: the workload's name and fields (with any overrides) plus `extra`."""
+    """The line's `config`: the workload's name and fields (with any overrides) plus `extra`;
+    both arms build it from the same workload, so their configs are equal."""
     return {"workload": name + ("" if not OVERRIDES else " (overridden)"),
             **{k: v for k, v in {**W.CONFIGS[name], **OVERRIDES}.items() if k != "seed"},
             **extra}
+
+
+def append_shape_bytes(name: str):
+    """(algorithmic bytes per call, device bytes per input copy) of an append workload, from its
+    fields alone (every slot of the workload is valid)."""
+    cfg = {**W.CONFIGS[name], **OVERRIDES}
+    T, H, D, P, N = cfg["T"], cfg["Hkv"], cfg["D"], cfg["page_size"], cfg["num_pages"]
+    alg = 2 * 2 * T * H * D * 2 + T * 8
+    dev = 2 * T * H * D * 2 + T * 8 + 2 * N * H * P * D * 2
+    return alg, dev
+
+
+def l2_note_bytes(alg: int, device_bytes: int) -> str:
+    n = copies_for(alg, device_bytes)
+    live = n * alg
+    where = ("exceed the {:.0f} MB L2" if live > L2_BYTES else
+             "fit in the {:.0f} MB L2 (a launch-bound small case)").format(L2_BYTES / 1e6)
+    return (f"{n} input copies alternated call by call; their live bytes ({live / 1e6:.1f} MB) "
+            f"{where}")
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return
     name = args.workload
+    threads = os.cpu_count() or 1
     if W.CONFIGS[name]["kind"] == "append":
         times = []
+        rows = 0
         for i in range(args.warmup + args.steps):
-            nbytes, secs, threads, rows = append_cpu_sample(name, 2.0)
+            nbytes, secs, _, rows = append_cpu_sample(name, 2.0)
             if i >= args.warmup:
                 times.append(secs / nbytes)
         per_byte = float(np.mean(times))
-        cfg = W.CONFIGS[name]
-        total = 2 * 2 * cfg["T"] * cfg["Hkv"] * cfg["D"] * 2 + cfg["T"] * 8
+        total, dev_bytes = append_shape_bytes(name)
         gbs = 1.0 / per_byte / 1e9
-        line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
-                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": round(total * per_byte * 1e3, 4), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16 copy", "data": "synthetic",
-                "config": workload_config(name, algorithmic_bytes_per_call=int(total),
-                                          l2="n/a (CPU)", parallelism="oracle on one host core"),
-                "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1,
-                                 "kind": "oracle", "sample": f"{rows} rows per step"},
-                "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
-        return
-    c = cpu_case(name)
-    per_step = max(0.2, 4.0 * args.cpu_budget / max(1, args.steps + args.warmup))
-    times = []
-    rows_used = 0
-    threads = os.cpu_count() or 1
-    for i in range(args.warmup + args.steps):
-        rows, secs, threads = oracle_sample_run(c, per_step)
-        if i >= args.warmup:
-            times.append(secs / rows)
-            rows_used = rows
-    per_row = float(np.mean(times))
-    secs_full = per_row * c.B * c.Hq
-    gbs = c.algorithmic_bytes() / secs_full / 1e9
+        ms = total * per_byte * 1e3
+        cores, dtype = 1, "bf16 copy"
+        sample = f"{rows} appended rows per step, scaled to the whole workload"
+        cfg = workload_config(name, algorithmic_bytes_per_call=int(total),
+                              l2=l2_note_bytes(total, dev_bytes), parallelism=f"replicas x{world}")
+    else:
+        c = cpu_case(name)
+        per_step = max(0.2, 4.0 * args.cpu_budget / max(1, args.steps + args.warmup))
+        times = []
+        rows_used = 0
+        for i in range(args.warmup + args.steps):
+            rows, secs, threads = oracle_sample_run(c, per_step)
+            if i >= args.warmup:
+                times.append(secs / rows)
+                rows_used = rows
+        per_row = float(np.mean(times))
+        secs_full = per_row * c.B * c.Hq
+        gbs = c.algorithmic_bytes() / secs_full / 1e9
+        ms = secs_full * 1e3
+        cores, dtype = threads, "f64"
+        sample = (f"{rows_used} of {c.B * c.Hq} (b, h) rows per step, scaled to the whole "
+                  f"workload")
+        cfg = workload_config(name, algorithmic_bytes_per_call=int(c.algorithmic_bytes()),
+                              l2=l2_note(c), parallelism=f"replicas x{world}")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(secs_full * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(name, algorithmic_bytes_per_call=int(c.algorithmic_bytes()),
-                                  l2="n/a (CPU)", parallelism="oracle on the host cores"),
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
-                         "kind": "oracle",
-                         "sample": f"{rows_used} of {c.B * c.Hq} (b, h) rows per step, scaled "
-                                   f"to the whole workload"},
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
+        "run": {"executor": "the fp64 oracle on the host cores, as it stands"},
     }
     print(json.dumps(line), flush=True)
 
@@ -484,8 +538,9 @@ def run_native(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     name = args.workload
-    cases = [make_case(name, dev, seed_offset=1000 * rank + k) for k in range(2)]
-    c0 = cases[0]
+    c0 = make_case(name, dev, rank=rank, copy=0)
+    ncopies = args.copies if args.copies > 0 else input_copies(c0)
+    cases = [c0] + [make_case(name, dev, rank=rank, copy=k) for k in range(1, ncopies)]
     if c0.kind == "append":
         ws = None
         outs = [c.k_pool for c in cases]
@@ -496,21 +551,39 @@ def run_native(args, world, rank, local):
         outs = [torch.empty(c.out_shape(), dtype=torch.bfloat16, device=dev) for c in cases]
     stream = torch.cuda.Stream(dev)
     alg = [c.algorithmic_bytes() for c in cases]
+    assert len(set(alg)) == 1, "input copies must share their structure"
+    bytes_call = float(alg[0])
+
+    def step(i):
+        B_.run_case(cases[i % ncopies], out=outs[i % ncopies], workspace=ws, stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            B_.run_case(cases[i % 2], out=outs[i % 2], workspace=ws, stream=stream)
+            step(i)
     stream.synchronize()
 
-    # ---- timed region: K back-to-back calls captured in one CUDA graph (so host launch cost is
-    # not in the device number), replayed between events on the launching stream
+    # ---- K back-to-back calls captured in one CUDA graph (host launch cost stays out of the
+    # device number); replayed R times between events on the launching stream
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for i in range(args.steps):
-            B_.run_case(cases[i % 2], out=outs[i % 2], workspace=ws, stream=stream)
+            step(i)
+    e_a = torch.cuda.Event(enable_timing=True)
+    e_b = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        graph.replay()                      # one untimed replay
+        graph.replay()                      # untimed: sizes R
+        e_a.record(stream)
+        graph.replay()
+        e_b.record(stream)
     stream.synchronize()
+    per_replay_s = max(e_a.elapsed_time(e_b) * 1e-3, 1e-6)
+    replays = int(max(1, math.ceil(args.min_seconds / per_replay_s)))
+    if world > 1:
+        replays = int(dist_max(float(replays), world, dev))
+    warm = int(max(1, math.ceil(min(1.0, args.min_seconds / 4) / per_replay_s)))
+    with torch.cuda.stream(stream):
+        for _ in range(warm):               # untimed: clocks settle under this load
+            graph.replay()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(gpu_selector(dev))
@@ -520,44 +593,47 @@ def run_native(args, world, rank, local):
     t_wall = time.perf_counter()
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        graph.replay()
+        for _ in range(replays):
+            graph.replay()
         ev1.record(stream)
     stream.synchronize()
     dist_barrier(world)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall
     clk = clocks.stop()
+    calls = args.steps * replays
     total_ms = ev0.elapsed_time(ev1)
-    step_ms = dist_max(total_ms / args.steps, world, dev)
-    launch_ms = total_ms / args.steps       # one kernel launch per step
-    bytes_step = float(np.mean([alg[i % 2] for i in range(args.steps)]))
+    step_ms = dist_max(total_ms / calls, world, dev)
+    launch_ms = total_ms / calls            # one kernel launch per call
 
     # ---- end to end: pinned host inputs copied in and the output copied back every step
-    hc = [HostCopy(c) for c in cases]
+    hc = HostCopy(c0)
     h2d = case_bytes_copied(c0)
     d2h = 0 if c0.kind == "append" else outs[0].numel() * 2
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(args.steps, 20))
     with torch.cuda.stream(stream):
-        hc[0].h2d(stream)
+        hc.h2d(stream, cases[0])
         B_.run_case(cases[0], out=outs[0], workspace=ws, stream=stream)
-        hc[0].d2h(outs[0])
+        hc.d2h(outs[0])
     stream.synchronize()
     dist_barrier(world)
     with torch.cuda.stream(stream):
         e_start.record(stream)
         for i in range(e2e_steps):
-            hc[i % 2].h2d(stream)
-            B_.run_case(cases[i % 2], out=outs[i % 2], workspace=ws, stream=stream)
-            hc[i % 2].d2h(outs[i % 2])
+            j = i % 2
+            hc.h2d(stream, cases[j])
+            B_.run_case(cases[j], out=outs[j], workspace=ws, stream=stream)
+            hc.d2h(outs[j])
         e_end.record(stream)
     stream.synchronize()
     e2e_ms = dist_max(e_start.elapsed_time(e_end) / e2e_steps, world, dev)
+    del hc
 
     peak, peak_kind = measured_peak()
-    value = world * bytes_step / (step_ms * 1e-3) / 1e9
-    achieved = bytes_step / (launch_ms * 1e-3) / 1e9
+    value = world * bytes_call / (step_ms * 1e-3) / 1e9
+    achieved = bytes_call / (launch_ms * 1e-3) / 1e9
     traffic = traffic_record(name)
     if rank != 0:
         return
@@ -569,20 +645,23 @@ def run_native(args, world, rank, local):
         "pct_of_nominal_8tbs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": workload_config(name, algorithmic_bytes_per_call=int(bytes_step),
-                                  algorithmic_bytes_per_copy=[int(a) for a in alg],
-                                  l2="inputs larger than L2; two input copies alternated",
+        "config": workload_config(name, algorithmic_bytes_per_call=int(bytes_call),
+                                  l2=l2_note(c0) if args.copies <= 0 else
+                                  f"{ncopies} input copies alternated (set by --copies)",
                                   parallelism=f"replicas x{world}"),
-        "e2e": {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "timing": {"graph_calls": args.steps, "replays": replays, "calls_timed": calls,
+                   "timed_ms": round(total_ms, 3), "untimed_warm_replays": warm,
+                   "input_copies": ncopies},
+        "e2e": {"value": round(world * bytes_call / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": args.steps,
+        "gpu_launches": calls,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs (burst copy)",
                      "kernel": kernel_label({**W.CONFIGS[name], **OVERRIDES}),
-                     "timing": "cuda graph of K calls",
-                     "launch_us": round(launch_ms * 1e3, 2)},
+                     "timing": f"cuda graph of {args.steps} calls replayed {replays} times",
+                     "launch_us": round(launch_ms * 1e3, 3)},
         "clocks": clk,
         "wall_s_timed_region": round(wall, 4),
     }
@@ -600,6 +679,11 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--copies", type=int, default=0,
+                    help="input copies to alternate (default: enough to exceed the L2 three "
+                         "times over); a small number keeps a profiler capture's memory small")
+    ap.add_argument("--min-seconds", type=float, default=4.0,
+                    help="length of the timed region (the K-call graph is replayed to fill it)")
     ap.add_argument("--override", action="append", metavar="KEY=VALUE",
                     help="change one field of the workload (e.g. B=8) for a smaller profiling case")
     args = ap.parse_args()

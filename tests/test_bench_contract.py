@@ -7,6 +7,7 @@ import subprocess
 import sys
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -39,6 +40,38 @@ def test_reference_line(workload):
         if k != "seed":
             assert cfg[k] == v
     assert cfg["algorithmic_bytes_per_call"] > 0
+
+
+@pytest.mark.parametrize("workload", ["dense_tiny", "append_paged"])
+def test_both_arms_build_the_same_config(workload):
+    """The native arm's config (the same workload fields, per-call bytes, L2 note and
+    parallelism, built from input copy 0 of rank 0) equals the reference arm's."""
+    import bench
+    ref = run_reference(workload)["config"]
+    if workload == "append_paged":
+        alg, dev = bench.append_shape_bytes(workload)
+        native = bench.workload_config(workload, algorithmic_bytes_per_call=int(alg),
+                                       l2=bench.l2_note_bytes(alg, dev), parallelism="replicas x1")
+    else:
+        c0 = bench.make_case(workload, "cpu")
+        native = bench.workload_config(workload, algorithmic_bytes_per_call=int(c0.algorithmic_bytes()),
+                                       l2=bench.l2_note(c0), parallelism="replicas x1")
+    assert native == ref
+
+
+def test_input_copies_share_structure():
+    """Input copies of one rank share their integer structure (so their byte counts are equal)
+    and differ in values."""
+    import bench
+    a = bench.make_case("dense_tiny", "cpu", copy=0)
+    b = bench.make_case("dense_tiny", "cpu", copy=1)
+    assert a.algorithmic_bytes() == b.algorithmic_bytes()
+    assert not torch.equal(a.q.view(torch.int16), b.q.view(torch.int16))
+    from token_decode_attention_split_gb300 import workloads as W
+    s0 = W.make_sparse(3, 8, 1, 64, 500, 300, 16, 100, seed=5)
+    s1 = W.make_sparse(3, 8, 1, 64, 500, 300, 16, 100, seed=5, value_seed=105)
+    assert torch.equal(s0.sel, s1.sel) and s0.n_valid_host == s1.n_valid_host
+    assert not torch.equal(s0.k_pool.view(torch.int16), s1.k_pool.view(torch.int16))
 
 
 def test_kernel_kind_follows_the_library_dispatch():

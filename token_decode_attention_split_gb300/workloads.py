@@ -18,7 +18,10 @@ Recipe (every value comes from ``torch.Generator(...).manual_seed(seed)``):
     ``0..window-1``, then distinct uniform pool rows from ``[window, pool_rows)``, then a seeded
     number in ``[0, max_pad]`` of trailing -1 pads.
 
-The five named workloads (``CONFIGS``) are the decode steps the attention kernels are measured on.
+The named workloads (``CONFIGS``) are the decode steps the attention kernels are measured on: the
+five decode configurations of the scope statement, two variants that route the same recipe
+through the other kernel instantiations (64-row pages, 16 query heads per KV head), the
+device-length and 4-token verify forms of the batched dense step, and the KV append.
 """
 from __future__ import annotations
 
@@ -45,9 +48,15 @@ CONFIGS = {
     # paged, per-sequence lengths in a device args buffer
     "paged_ragged": dict(kind="paged", B=64, Hq=32, Hkv=8, D=128, page_size=16, num_pages=160000,
                          kv_min=128, kv_max=32768, seed=1004),
+    # the same paged step with 64-row pages: one KV head per unit (the single-head paged kernel)
+    "paged_ragged_p64": dict(kind="paged", B=64, Hq=32, Hkv=8, D=128, page_size=64,
+                             num_pages=40000, kv_min=128, kv_max=32768, seed=1009),
     # sparse, fixed-width int32 selection with trailing -1 pads
     "sparse_selected": dict(kind="sparse", B=32, Hq=64, Hkv=1, D=128, pool_rows=65536, width=2048,
                             window=128, max_pad=512, seed=1005),
+    # the same selection recipe with 4 KV heads of 16 query heads each (the warp-MMA sparse kernel)
+    "sparse_selected_g16": dict(kind="sparse", B=32, Hq=64, Hkv=4, D=128, pool_rows=65536,
+                                width=2048, window=128, max_pad=512, seed=1010),
     # KV append into the paged cache (the step before paged decode): a ctx window of new rows
     "append_paged": dict(kind="append", T=8192, Hkv=8, D=128, page_size=16, num_pages=160000,
                          seed=1006),
@@ -73,10 +82,13 @@ def _normal_bf16(shape, gen: torch.Generator, device, mult: float = 1.0, chunk_r
     return out
 
 
-def _gens(seed: int, device):
+def _gens(seed: int, device, value_seed=None):
+    """Generators of one case: float values from ``value_seed`` (default ``seed``) on the device,
+    integer structure (lengths, pages, selections, slots) from ``seed`` on the CPU, so two cases
+    with one ``seed`` and different ``value_seed`` share their structure and byte counts."""
     dev = torch.device(device)
     g_dev = torch.Generator(device=dev)
-    g_dev.manual_seed(seed)
+    g_dev.manual_seed(seed if value_seed is None else value_seed)
     g_cpu = torch.Generator()
     g_cpu.manual_seed(seed + 7919)
     return dev, g_dev, g_cpu
@@ -196,10 +208,11 @@ class AppendCase:
         return 2 * 2 * valid * self.Hkv * self.D * 2 + self.T * 8
 
 
-def make_append(T, Hkv, D, page_size, num_pages, seed, device="cpu", pad_every=0) -> AppendCase:
+def make_append(T, Hkv, D, page_size, num_pages, seed, device="cpu", pad_every=0,
+                value_seed=None) -> AppendCase:
     """T new rows to distinct random slots of a paged pool; with pad_every = n, every n-th slot
     is -1 (a padding row)."""
-    dev, g, gc = _gens(seed, device)
+    dev, g, gc = _gens(seed, device, value_seed)
     if T > num_pages * page_size:
         raise ValueError("more rows than slots")
     slots = torch.randperm(num_pages * page_size, generator=gc)[:T].to(torch.int64)
@@ -213,10 +226,11 @@ def make_append(T, Hkv, D, page_size, num_pages, seed, device="cpu", pad_every=0
 
 
 def make_dense(B, Hq, Hkv, D, capacity, k_len, seed, device="cpu", k_scale=1.0,
-               poison_tail=False, scale=None, sq=1, causal=0, device_len=False) -> DenseCase:
+               poison_tail=False, scale=None, sq=1, causal=0, device_len=False,
+               value_seed=None) -> DenseCase:
     """sq > 1: several query tokens per sequence (q [B, Hq, sq, D]); device_len: the length is
     also stored as one u32 word in device memory, for the call that reads it there."""
-    dev, g, _ = _gens(seed, device)
+    dev, g, _ = _gens(seed, device, value_seed)
     q = _normal_bf16((B, Hq, sq, D), g, dev)
     k = _normal_bf16((B, Hkv, capacity, D), g, dev, mult=k_scale)
     v = _normal_bf16((B, Hkv, capacity, D), g, dev)
@@ -230,8 +244,8 @@ def make_dense(B, Hq, Hkv, D, capacity, k_len, seed, device="cpu", k_scale=1.0,
 
 def make_paged(B, Hq, Hkv, D, page_size, num_pages, kv_min, kv_max, seed, device="cpu",
                kv_len_stride=1, max_pages=None, kv_lens=None, poison_unused=True,
-               shuffle_pages=True, scale=None) -> PagedCase:
-    dev, g, gc = _gens(seed, device)
+               shuffle_pages=True, scale=None, value_seed=None) -> PagedCase:
+    dev, g, gc = _gens(seed, device, value_seed)
     if kv_lens is None:
         kv_lens = torch.randint(kv_min, kv_max + 1, (B,), generator=gc).tolist()
     kv_lens = [int(x) for x in kv_lens]
@@ -274,8 +288,8 @@ def make_paged(B, Hq, Hkv, D, page_size, num_pages, kv_min, kv_max, seed, device
 
 
 def make_sparse(B, Hq, Hkv, D, pool_rows, width, window, max_pad, seed, device="cpu",
-                poison_unselected=False, scale=None) -> SparseCase:
-    dev, g, gc = _gens(seed, device)
+                poison_unselected=False, scale=None, value_seed=None) -> SparseCase:
+    dev, g, gc = _gens(seed, device, value_seed)
     if window > width or window > pool_rows:
         raise ValueError("window larger than the selection or the pool")
     sel = torch.full((B, width), -1, dtype=torch.int32)
