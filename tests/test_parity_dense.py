@@ -100,19 +100,17 @@ def test_workspace_too_small_is_rejected():
 
 @pytest.mark.parametrize("name", ["dense_tiny", "dense_batched", "dense_long"])
 def test_dense_named_workloads(name):
-    """Full sizes: sampled (b, h) rows against the oracle, every row checked for properties that
-    hold at any size (finite, inside the per-column range of the attended V rows)."""
+    """Full sizes, in the launch configuration the benchmark times: every (b, h) row against the
+    oracle (the stream-K schedule splits units at points that depend on the totals, so every
+    row's split and merge path is checked), and every row inside the per-column range of the
+    attended V rows."""
     c = W.make(name, device=DEV)
     out = B_.run_case(c)
     torch.cuda.synchronize()
     got = out_f64(out)
-    n = c.B * c.Hq
-    rng = np.random.default_rng(0)
-    pairs = np.unique(np.concatenate([[0, n - 1], rng.choice(n, size=min(n, 24), replace=False)]))
     host = W.DenseCase(c.q.cpu(), c.k.cpu(), c.v.cpu(), c.k_len, c.scale, c.B, c.Hq, c.Hkv, c.D,
                        c.capacity)
-    ref = oracle_for(host, pairs=pairs)
-    assert_close(got.reshape(n, -1)[pairs], ref.reshape(n, -1)[pairs], name)
+    assert_close(got, oracle_for(host), name)
     assert np.all(np.isfinite(got))
     G = c.Hq // c.Hkv
     live = c.v[:, :, :c.k_len].float()
@@ -163,16 +161,13 @@ def test_device_len_graph_replay_follows_the_length_word():
 
 
 def test_named_device_len_workload():
-    """dense_device_len at full size: the length word on the device, sampled rows vs the oracle."""
+    """dense_device_len at full size: the length word on the device, every row vs the oracle."""
     c = W.make("dense_device_len", device=DEV)
     out = B_.run_case(c)
     torch.cuda.synchronize()
-    n = c.B * c.Hq
-    pairs = np.unique(np.concatenate([[0, n - 1], np.random.default_rng(1).choice(n, 24, replace=False)]))
     host = W.DenseCase(c.q.cpu(), c.k.cpu(), c.v.cpu(), c.k_len, c.scale, c.B, c.Hq, c.Hkv, c.D,
                        c.capacity)
-    assert_close(out_f64(out).reshape(n, -1)[pairs], oracle_for(host, pairs=pairs).reshape(n, -1)[pairs],
-                 "dense_device_len")
+    assert_close(out_f64(out), oracle_for(host), "dense_device_len")
 
 
 def test_spec_wrapper_matches_the_plain_call():

@@ -86,13 +86,10 @@ def test_no_device_error_recorded():
 
 
 def test_named_verify_workload():
-    """dense_verify4 at full size (4 query tokens, causal): the first and last sequences against
-    the oracle, every output finite."""
+    """dense_verify4 at full size (4 query tokens, causal): every sequence against the oracle."""
     c = W.make("dense_verify4", device=DEV)
     out = B_.run_case(c)
     torch.cuda.synchronize()
     assert out.shape == (c.B, c.Hq, 4, c.D) and torch.isfinite(out.float()).all()
-    for b in (0, c.B - 1):
-        ref = oracle.dense_mq(c.q[b:b + 1].cpu(), c.k[b:b + 1].cpu(), c.v[b:b + 1].cpu(), c.k_len,
-                              c.scale, causal=True)
-        assert_close(f64(out[b:b + 1]), ref, f"dense_verify4 b={b}")
+    ref = oracle.dense_mq(c.q.cpu(), c.k.cpu(), c.v.cpu(), c.k_len, c.scale, causal=True)
+    assert_close(f64(out), ref, "dense_verify4")

@@ -127,30 +127,29 @@ def test_paged_graph_replay_reads_lengths_on_device():
         assert_close(got, oracle_for(c), f"replay {new}")
 
 
-def test_paged_named_workload():
-    """The full paged_ragged workload: sampled sequences compared against the oracle on a
-    compact host copy of their pages; all rows finite."""
-    c = W.make("paged_ragged", device=DEV)
+@pytest.mark.parametrize("name", ["paged_ragged", "paged_ragged_p64"])
+def test_paged_named_workload(name):
+    """The full paged workloads (16-row pages: units of four KV heads; 64-row pages: one KV head
+    per unit), in the launch configuration the benchmark times: every sequence's every row
+    against the oracle, on a compact host copy of the pages the sequences use."""
+    c = W.make(name, device=DEV)
     out = B_.run_case(c)
     torch.cuda.synchronize()
     got = out_f64(out)
     assert np.all(np.isfinite(got))
-    rng = np.random.default_rng(1)
     lens = c.live_lengths()
-    pick = sorted(set([int(np.argmin(lens)), int(np.argmax(lens))] +
-                      rng.choice(c.B, 6, replace=False).tolist()))
     bt = c.block_table.cpu()
-    for b in pick:
-        n = lens[b]
-        npg = -(-n // c.page_size)
-        pages = bt[b, :npg].long().to(DEV)
-        kp = c.k_pool.index_select(0, pages).cpu()
-        vp = c.v_pool.index_select(0, pages).cpu()
-        sub = W.PagedCase(c.q[b:b + 1].cpu(), kp, vp,
-                          torch.arange(npg, dtype=torch.int32).reshape(1, npg),
-                          torch.tensor([n], dtype=torch.int32), 1, [n], c.scale, 1, c.Hq, c.Hkv,
-                          c.D, c.page_size, npg)
-        assert_close(got[b:b + 1], oracle_for(sub), f"paged_ragged b={b}")
+    npg = [-(-n // c.page_size) for n in lens]
+    first = np.concatenate([[0], np.cumsum(npg)[:-1]]).astype(np.int64)
+    pages = torch.cat([bt[b, :npg[b]].long() for b in range(c.B)]).to(DEV)
+    kp = c.k_pool.index_select(0, pages).cpu()
+    vp = c.v_pool.index_select(0, pages).cpu()
+    table = torch.zeros((c.B, max(npg)), dtype=torch.int32)
+    for b in range(c.B):
+        table[b, :npg[b]] = torch.arange(first[b], first[b] + npg[b], dtype=torch.int32)
+    host = W.PagedCase(c.q.cpu(), kp, vp, table, torch.tensor(lens, dtype=torch.int32), 1, lens,
+                       c.scale, c.B, c.Hq, c.Hkv, c.D, c.page_size, int(pages.numel()))
+    assert_close(got, oracle_for(host), name)
 
 
 def test_no_device_error_recorded():

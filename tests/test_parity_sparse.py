@@ -149,21 +149,23 @@ def test_sparse_width_zero_gives_zeros():
     assert torch.count_nonzero(out).item() == 0
 
 
-def test_sparse_named_workload():
-    """The full sparse_selected workload, every output row against the oracle, and the same call
-    with each sequence's pads removed is bit-identical."""
-    c = W.make("sparse_selected", device=DEV)
+@pytest.mark.parametrize("name", ["sparse_selected", "sparse_selected_g16"])
+def test_sparse_named_workload(name):
+    """The full sparse workloads (64 query heads per KV head: the tensor-core kernel; 16: the
+    warp-MMA kernel), every output row against the oracle, and for every sequence the same call
+    with its pads removed is bit-identical."""
+    c = W.make(name, device=DEV)
     out = B_.run_case(c)
     torch.cuda.synchronize()
     host = W.SparseCase(c.q.cpu(), c.k_pool.cpu(), c.v_pool.cpu(), c.sel.cpu(), c.scale, c.B,
                         c.Hq, c.Hkv, c.D, c.pool_rows, c.n_valid_host)
-    assert_close(out_f64(out), oracle_for(host), "sparse_selected")
-    for b in (0, 7, 31):
+    assert_close(out_f64(out), oracle_for(host), name)
+    for b in range(c.B):
         n = c.n_valid_host[b]
         sub = W.SparseCase(c.q[b:b + 1], c.k_pool[b:b + 1], c.v_pool[b:b + 1],
                            c.sel[b:b + 1, :n].contiguous(), c.scale, 1, c.Hq, c.Hkv, c.D,
                            c.pool_rows, [n])
-        assert torch.equal(B_.run_case(sub), out[b:b + 1])
+        assert torch.equal(B_.run_case(sub), out[b:b + 1]), f"{name}: pads of b={b} not neutral"
 
 
 def test_no_device_error_recorded():
