@@ -29,10 +29,11 @@
  *       sel             int32 [B, width], shared by every KV head of a sequence
  *   - Supported: D in {64, 128}; 1 <= Hq / Hkv <= 64.  Other shapes return DA_ERR_UNSUPPORTED
  *     (fail closed, nothing launched).
- *   - Streams: a call only enqueues kernels on `stream` (a cudaStream_t; NULL is the legacy
- *     default stream).  It allocates nothing, frees nothing and never synchronises, so it can be
- *     captured in a CUDA graph; the tensor-map descriptors and launch arguments it builds are
- *     baked into the launch.
+ *   - Streams: a call only enqueues work on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  It allocates nothing, frees nothing and never synchronises.  The calls
+ *     that take a caller-owned workspace, and the append calls, can therefore be captured in a
+ *     CUDA graph; the tensor-map descriptors and launch arguments they build are baked into the
+ *     launch.
  *   - Values that live on the device (kv_lens, block_table, sel) are never checked by a
  *     device-to-host copy.  They are handled on the device: kv_len is clamped to
  *     max_pages_per_seq * page_size; a row whose block-table entry lies outside [0, num_pages),
@@ -249,10 +250,9 @@ da_status decode_attn_check_wait_timeout(uint32_t limit_us, void *stream);
 /*
  * decode_attn_dense without a workspace argument, for callers that cannot allocate device memory
  * where they call it: a plugin or custom operator inside a host framework that owns every device
- * allocation and passes the operator only its inputs and outputs; code issuing work while a
- * stream is being captured into a CUDA graph, where cudaMalloc is not allowed; latency-critical
- * decode loops, where cudaMalloc may synchronise the device; processes that reserve nearly all
- * HBM up front.  No counterpart in the pages: this entry point is an addition of this library.
+ * allocation and passes the operator only its inputs and outputs; latency-critical decode loops,
+ * where cudaMalloc may synchronise the device; processes that reserve nearly all HBM up front.
+ * No counterpart in the pages: this entry point is an addition of this library.
  *
  * Same arguments, layouts and results as decode_attn_dense, minus the workspace: the scratch is a
  * file-scope device array of DECODE_ATTN_NOALLOC_SCRATCH_BYTES bytes inside the library.
@@ -260,12 +260,13 @@ da_status decode_attn_check_wait_timeout(uint32_t limit_us, void *stream);
  *     size return DA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
  *   - Every call shares the array: calls that can overlap on the GPU (different streams, or
  *     several host threads on one device) race on it and must be serialised by the caller.
- *   - Each call first clears, on `stream`, the part of the array it uses (the merge counters
- *     must start at zero and the array keeps the previous call's contents); this clearing is the
- *     only work it enqueues besides the kernel, and an argument error found after it leaves
- *     nothing but the cleared scratch behind.
- *   - The first call on each device looks up the array's device address (once, with that device
- *     current) and caches it; make that first call before any stream capture on the device.
+ *   - The array keeps the previous call's contents, so each call clears its merge counters (the
+ *     part that must start at zero) on `stream` right before its kernel; that clearing and the
+ *     kernel are all it enqueues, and a call rejected by an argument check enqueues nothing.
+ *   - The first call on each device looks up the array's device address (with that device
+ *     current) and caches it; make that first call before any stream capture on the device.  The
+ *     cache belongs to the CUDA context: after a device reset the next call looks it up again
+ *     (that call, too, should come before any stream capture).
  *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  */
 da_status decode_attn_dense_noalloc(const void *q, const void *k, const void *v, void *out, int B,

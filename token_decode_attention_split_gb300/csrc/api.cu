@@ -25,9 +25,12 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_grid_limit{0};
 std::mutex g_mu;
-std::set<std::pair<const void*, int>> g_configured;   // (kernel, device) with smem opt-in done
+// (kernel, context id) pairs whose shared-memory opt-in is done: the attribute belongs to the
+// module loaded in that context, so a device reset (a new primary context) needs it again
+std::set<std::pair<const void*, unsigned long long>> g_configured;
 int g_sm_count[kMaxDevices];                          // 0 = not queried yet
 unsigned* g_err_ptr[kMaxDevices];
+unsigned long long g_err_ctx[kMaxDevices];            // context the cached address belongs to
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -45,6 +48,19 @@ EncodeTiledFn encode_fn() {
         return reinterpret_cast<EncodeTiledFn>(f);
     }();
     return fn;
+}
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(f);
 }
 
 int current_device() {
@@ -66,10 +82,12 @@ int sm_count(int dev) {
 
 unsigned* device_error_ptr(int dev) {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_err_ptr[dev] == nullptr) {
+    const unsigned long long ctx = current_context_id();
+    if (g_err_ptr[dev] == nullptr || ctx == 0 || ctx != g_err_ctx[dev]) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_device_error_word) != cudaSuccess) return nullptr;
         g_err_ptr[dev] = static_cast<unsigned*>(ptr);
+        g_err_ctx[dev] = current_context_id();
     }
     return g_err_ptr[dev];
 }
@@ -191,19 +209,32 @@ long long sparse_chunks(long long width) {
 
 }  // namespace
 
+unsigned long long current_context_id() {
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
 cudaError_t launch_kernel(const void* kernel, int smem, const Launch& L) {
     const int dev = current_device();
     if (dev < 0) return cudaErrorInvalidDevice;
-    bool need = false;
-    {
+    const unsigned long long ctx = current_context_id();
+    bool need = true;
+    if (ctx != 0) {
         std::lock_guard<std::mutex> lk(g_mu);
-        need = g_configured.find({kernel, dev}) == g_configured.end();
+        need = g_configured.find({kernel, ctx}) == g_configured.end();
     }
     if (need) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        std::lock_guard<std::mutex> lk(g_mu);
-        g_configured.insert({kernel, dev});
+        if (ctx != 0) {
+            std::lock_guard<std::mutex> lk(g_mu);
+            g_configured.insert({kernel, ctx});
+        }
     }
     void* args[] = {const_cast<CUtensorMap*>(&L.tm_k), const_cast<CUtensorMap*>(&L.tm_v),
                     const_cast<Params*>(&L.p)};
@@ -338,7 +369,7 @@ namespace {
 da_status run_dense(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
                     int D, int64_t capacity, int64_t k_len, const uint32_t* k_len_dev,
                     float softmax_scale, void* workspace, size_t workspace_bytes, void* stream,
-                    int sq = 1, int causal = 0) {
+                    int sq = 1, int causal = 0, bool clear_workspace = false) {
     da_status st = check_common(q, out, B, Hq, Hkv, D, softmax_scale, workspace);
     if (st != DA_OK) return st;
     if (sq < 1) return DA_ERR_INVALID_ARGUMENT;
@@ -391,10 +422,26 @@ da_status run_dense(const void* q, const void* k, const void* v, void* out, int 
     L.grid = static_cast<int>(std::min<long long>(persistent_ctas(dev), spread));
     L.stream = cs;
     L.threads = Roles<kDense>::kThreads;
+    // the merge counters are all that must start at zero (partial rows are written before any
+    // CTA reads them)
+    if (clear_workspace && cudaMemsetAsync(workspace, 0, w.lse - w.counters, cs) != cudaSuccess)
+        return DA_ERR_CUDA;
     return launch_dense(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }
 
 }  // namespace
+
+namespace da {
+
+da_status dense_clearing_workspace(const void* q, const void* k, const void* v, void* out, int B,
+                                   int Hq, int Hkv, int D, int64_t capacity, int64_t k_len,
+                                   float softmax_scale, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+    return run_dense(q, k, v, out, B, Hq, Hkv, D, capacity, k_len, nullptr, softmax_scale,
+                     workspace, workspace_bytes, stream, 1, 0, true);
+}
+
+}  // namespace da
 
 extern "C" {
 

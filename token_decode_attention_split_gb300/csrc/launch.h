@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "decode_kernel.cuh"
+#include "host_api.h"
 
 namespace da {
 
@@ -35,7 +36,8 @@ cudaError_t launch_sparse_tc(int D, const Launch& L);
 cudaError_t launch_wait_check(unsigned* err, uint64_t limit_ns, cudaStream_t stream);
 
 // Opts the kernel into `smem` bytes of dynamic shared memory on the current device (once per
-// kernel and device), then launches it with L.threads threads per block.
+// kernel and CUDA context), then launches it with L.threads threads per block.
 cudaError_t launch_kernel(const void* kernel, int smem, const Launch& L);
+
 
 }  // namespace da
