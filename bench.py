@@ -665,6 +665,10 @@ def run_native(args, world, rank, local):
         "clocks": clk,
         "wall_s_timed_region": round(wall, 4),
     }
+    if c0.kind == "append":
+        line["roofline"]["traffic_note"] = (
+            "DRAM reads and the writes that left L2 before the captured launch ended; the "
+            "scattered pool writes are mostly still dirty in L2 then, so this is about the reads")
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(name, args.cpu_budget)
     print(json.dumps(line), flush=True)

@@ -102,6 +102,10 @@ TC_CASES = [
     (3, 33, 1, 3000, 1100, 32, 90),   # G = 33: one live lane in the second softmax warp
     (2, 80, 2, 3000, 900, 32, 400),   # G = 40, two units per sequence
     (2, 128, 2, 4000, 1600, 64, 200), # G = 64, two units per sequence, four chunks
+    (2, 64, 1, 8000, 2048, 16, 0),    # exactly four chunks: the last tc_merge case
+    (2, 64, 1, 8000, 2049, 16, 0),    # five chunks: merge_unit
+    (2, 64, 1, 8000, 3000, 32, 100),  # six chunks
+    (1, 96, 2, 12000, 6000, 16, 300), # G = 48, twelve chunks
 ]
 
 
@@ -139,6 +143,22 @@ def test_sparse_tensor_core_pad_tiles_and_empty_chunk():
     c.sel = sel
     out = B_.run_case(c)
     assert_close(out_f64(out), oracle_for(c), "pad tiles / empty chunk")
+
+
+@pytest.mark.parametrize("G,D", [(64, 128), (40, 64)])
+def test_pads_bit_identical_across_the_two_merges(G, D):
+    """Up to four chunks merge in tc_merge (rows fetched by bulk copies), more in merge_unit; both
+    perform the same operations in the same order, so a selection padded from four chunks to ten
+    gives the bits of the call without the pads."""
+    c = W.make_sparse(3, G, 1, D, 8000, 2000, 64, 500, seed=70 + G, device=DEV,
+                      poison_unselected=True)
+    ref = B_.run_case(c)                        # up to four chunks: tc_merge
+    more = torch.cat([c.sel, torch.full((c.B, 3000), -1, dtype=torch.int32, device=DEV)], dim=1)
+    wide = W.SparseCase(c.q, c.k_pool, c.v_pool, more.contiguous(), c.scale, c.B, c.Hq, c.Hkv,
+                        c.D, c.pool_rows, c.n_valid_host)
+    out = B_.run_case(wide)                     # ten chunks: merge_unit
+    assert torch.equal(out, ref)
+    assert_close(out_f64(out), oracle_for(c), f"G={G} D={D}")
 
 
 def test_sparse_width_zero_gives_zeros():
