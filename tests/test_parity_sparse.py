@@ -161,6 +161,20 @@ def test_pads_bit_identical_across_the_two_merges(G, D):
     assert_close(out_f64(out), oracle_for(c), f"G={G} D={D}")
 
 
+@pytest.mark.parametrize("width", [2000, 1600, 6000])
+def test_sparse_tensor_core_counters_return_to_zero(width):
+    """Every call leaves the workspace's merge counters (one word per unit) at zero, and a second
+    call on the same workspace gives the same bits."""
+    c = W.make_sparse(4, 64, 1, 128, 8000, width, 32, 200, seed=80 + width, device=DEV)
+    ws = B_.new_workspace(B_.decode_attn_workspace_size(2, c.B, c.Hq, c.Hkv, c.D, c.width), DEV)
+    a = B_.run_case(c, workspace=ws)
+    b = B_.run_case(c, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert torch.count_nonzero(ws[: 4 * c.B * c.Hkv]).item() == 0
+    assert_close(out_f64(a), oracle_for(c), f"width {width}")
+
+
 def test_sparse_width_zero_gives_zeros():
     c = W.make_sparse(2, 8, 1, 128, 100, 8, 2, 0, seed=45, device=DEV)
     c.sel = c.sel[:, :0].contiguous()

@@ -110,6 +110,19 @@ static_assert(sizeof(TcBars) <= 1024, "barrier block");
 // kHeadsPerInstr heads (lane = one float4 column of one of them), and a thread takes its heads
 // four at a time with every load of a pass in flight.  The caller has acquired every segment's
 // rows (the unit's counter) before the call.
+// pick ? a : b, component by component, as a select instruction (kept a select, so that a chain
+// of them over a register array never becomes an indexed access to local memory)
+__device__ __forceinline__ float4 select4(bool pick, const float4& a, const float4& b) {
+    float4 r;
+    asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %8, 0;\n\t"
+        "selp.f32 %0, %4, %9, q;\n\tselp.f32 %1, %5, %10, q;\n\t"
+        "selp.f32 %2, %6, %11, q;\n\tselp.f32 %3, %7, %12, q;\n\t}"
+        : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+        : "f"(a.x), "f"(a.y), "f"(a.z), "f"(a.w), "r"(static_cast<unsigned>(pick)), "f"(b.x),
+          "f"(b.y), "f"(b.z), "f"(b.w));
+    return r;
+}
+
 template <int D>
 __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, float* w_sm,
                                          unsigned char* rows_sm, uint64_t* mrows, int hq0, int G,
@@ -128,9 +141,11 @@ __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, fl
     const float4* src =
         reinterpret_cast<const float4*>(p.part_o) + static_cast<size_t>(first_seg) * SH * D4;
     const float4* rs = reinterpret_cast<const float4*>(rows_sm);
-    float* h_inv = w_sm + kTcMergeSegments * 64;             // [64]
-    int* h_live = reinterpret_cast<int*>(h_inv + 64);        // [64]
-    int* h_only = h_live + 64;                               // [64]
+    // per head h: its segments' weights in w4[h] and {1 / sum, live count, last live segment}
+    // in h_meta[h], one 16-byte load each
+    static_assert(kTcMergeSegments == 4, "one float4 of weights per head");
+    float4* w4 = reinterpret_cast<float4*>(w_sm);            // [64]
+    float4* h_meta = w4 + 64;                                // [64]
     if (tid == 0) {
         fence_proxy_async_global();
         mbar_arrive_expect_tx(mrows, nseg * seg_bytes);
@@ -148,20 +163,20 @@ __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, fl
         }
         float L = 0.f;
         int live = 0, only = 0;
+        float w[kTcMergeSegments];
 #pragma unroll
         for (int k = 0; k < kTcMergeSegments; ++k) {
-            float w = 0.f;
+            w[k] = 0.f;
             if (l[k] != -CUDART_INF_F) {
-                w = fast_exp2(l[k] - M);
-                L = live ? L + w : w;
+                w[k] = fast_exp2(l[k] - M);
+                L = live ? L + w[k] : w[k];
                 ++live;
                 only = k;
             }
-            w_sm[k * 64 + tid] = w;
         }
-        h_inv[tid] = live ? 1.0f / L : 0.f;
-        h_live[tid] = live;
-        h_only[tid] = only;
+        w4[tid] = make_float4(w[0], w[1], w[2], w[3]);
+        h_meta[tid] = make_float4(live ? 1.0f / L : 0.f, __int_as_float(live),
+                                  __int_as_float(only), 0.f);
     }
     if (!mbar_wait_warp(mrows, 0, sm.abort)) {
         *sm.abort = 1;
@@ -178,24 +193,29 @@ __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, fl
     for (int j0 = 0; j0 < kHeadsPerThread; j0 += kPass) {
         int live[kPass], only[kPass];
         float inv[kPass];
+        float w[kTcMergeSegments][kPass];
 #pragma unroll
         for (int j = 0; j < kPass; ++j) {
-            const int h = min(head_of(j0 + j), G - 1);
-            live[j] = h_live[h];
-            only[j] = h_only[h];
-            inv[j] = h_inv[h];
+            const int hj = head_of(j0 + j);
+            const int h = min(hj, G - 1);
+            const float4 m = h_meta[h];
+            const float4 wj = w4[h];
+            inv[j] = m.x;
+            live[j] = __float_as_int(m.y);
+            only[j] = __float_as_int(m.z);
+            // a head past G contributes nothing (its store is skipped too)
+            w[0][j] = hj < G ? wj.x : 0.f;
+            w[1][j] = hj < G ? wj.y : 0.f;
+            w[2][j] = hj < G ? wj.z : 0.f;
+            w[3][j] = hj < G ? wj.w : 0.f;
         }
-        float w[kTcMergeSegments][kPass];
         float4 o[kTcMergeSegments][kPass];
 #pragma unroll
         for (int k = 0; k < kTcMergeSegments; ++k)
 #pragma unroll
             for (int j = 0; j < kPass; ++j) {
-                const int hj = head_of(j0 + j);
-                const int h = min(hj, G - 1);
-                const int kk = min(k, nseg - 1);
-                w[k][j] = (k < nseg && hj < G) ? w_sm[kk * 64 + h] : 0.f;
-                o[k][j] = rs[(kk * G + h) * D4 + c];
+                const int h = min(head_of(j0 + j), G - 1);
+                o[k][j] = rs[(min(k, nseg - 1) * G + h) * D4 + c];
             }
 #pragma unroll
         for (int j = 0; j < kPass; ++j) {
@@ -207,7 +227,10 @@ __device__ __forceinline__ bool tc_merge(const Params& p, const SmemPtrs& sm, fl
                 acc = w[k][j] != 0.f ? f : acc;
             }
             const int h = head_of(j0 + j);
-            const float4 single = rs[(only[j] * G + min(h, G - 1)) * D4 + c];
+            float4 single = o[0][j];
+#pragma unroll
+            for (int k = 1; k < kTcMergeSegments; ++k)
+                single = select4(k == only[j], o[k][j], single);
             const float4 scaled =
                 make_float4(acc.x * inv[j], acc.y * inv[j], acc.z * inv[j], acc.w * inv[j]);
             const float4 v =
@@ -432,10 +455,12 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
             *reinterpret_cast<uint4*>(qs + (c >> 3) * (kTcM * 128) + r * 128 +
                                       (((c ^ r) & 7) << 4)) = v[k];
         }
+        // (each thread starts at its own swizzled 16-byte slot, so the eight rows a quarter warp
+        // writes at once fall in different banks)
         if (!live)
             for (int i = 0; i < 2 * (kTileKeys / 8); ++i)
                 *reinterpret_cast<uint4*>(base + Tg::kOffP + (i >> 3) * kTcPBytes + h * 128 +
-                                          (i & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                                          (((i ^ h) & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
         mbar_arrive(&bar.q_ready);
     }
