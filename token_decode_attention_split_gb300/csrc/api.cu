@@ -195,7 +195,7 @@ int persistent_ctas(int dev) {
     return (lim > 0 && lim < sms) ? lim : sms;
 }
 
-// Sparse work split: one CTA per (sequence and KV head, chunk of 512 selection entries) with all
+// Sparse work split: items of (sequence and KV head, chunk of 512 selection entries) with all
 // of the unit's G <= 64 query heads.  33..64 heads run on the tensor-core kernel, up to 32 on the
 // mma.sync kernel (which holds at most 32 query columns).  The chunk depends on nothing, not on
 // the width, B or the device, so trailing pads never move a chunk boundary.
@@ -600,12 +600,15 @@ da_status decode_attn_sparse(const void* q, const void* k_pool, const void* v_po
     L.p.seg_heads = G;
     L.p.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
     L.p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
-    L.grid = static_cast<int>(units * chunks);
     L.stream = cs;
     if (sparse_uses_tc(G, D)) {
+        // one CTA per (unit, chunk)
+        L.grid = static_cast<int>(units * chunks);
         L.threads = sparse_tc_threads();
         return launch_sparse_tc(D, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
     }
+    // persistent: each CTA takes a contiguous range of whole (unit, chunk) items
+    L.grid = static_cast<int>(std::min<long long>(persistent_ctas(dev), units * chunks));
     L.threads = Roles<kSparse>::kThreads;
     return launch_sparse(D, GP, L) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }

@@ -9,9 +9,11 @@
 // Dense and paged calls run a persistent grid (one CTA per SM): the tiles of all units are laid
 // end to end and CTA c takes the contiguous range [c*N/C, (c+1)*N/C), so the load is balanced to
 // one tile whatever the lengths.  Sparse calls (up to 32 query heads per KV head; larger groups
-// run on the tensor-core kernel) give each CTA one unit over one chunk of 512 selection entries:
-// the chunk is fixed, so trailing -1 pads cannot move a chunk boundary.  Each CTA's piece of a
-// unit is a "segment".
+// run on the tensor-core kernel) cut each unit's selection into chunks of 512 entries — fixed, so
+// trailing -1 pads cannot move a chunk boundary — and also run a persistent grid: the (unit,
+// chunk) items are numbered end to end and CTA c takes a contiguous range of whole items, each
+// finished as its own segment while the producers already gather the next item's rows.  Each
+// CTA's piece of a unit is a "segment".
 //
 // Inside a CTA.  The producer warps (one for dense, two taking alternate tiles for paged, four
 // sharing every tile for sparse) stream K and V tiles into a ring of shared-memory stages (TMA
@@ -893,23 +895,32 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         t0 = static_cast<int>(static_cast<long long>(blockIdx.x) * N / C);
         t1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * N / C);
     }
-    // sparse: this CTA's chunk of one unit; blockIdx.x = u * nchunks + chunk
-    int sp_u = 0, sp_key0 = 0, sp_nkeys = 0;
+    // sparse: the items (unit u, chunk) are numbered u * nchunks + chunk; CTA c takes the
+    // contiguous range [c * I / C, (c + 1) * I / C) of the I items, each a whole chunk (so a
+    // chunk boundary never moves) finished as its own segment
+    int it_begin = 0, it_end = 0;
     if (VAR == kSparse) {
-        sp_u = blockIdx.x / p.nchunks;
-        const int chunk = blockIdx.x - sp_u * p.nchunks;
-        sp_key0 = chunk * kSparseChunkUnit;
-        sp_nkeys = min(kSparseChunkUnit, p.width - sp_key0);
-        t0 = sp_key0 / kTileKeys;
-        t1 = (sp_key0 + sp_nkeys + kTileKeys - 1) / kTileKeys;
+        const int I = p.B * p.Hkv * p.nchunks;
+        C = min(static_cast<int>(gridDim.x), I);
+        if (static_cast<int>(blockIdx.x) < C) {
+            it_begin = static_cast<int>(static_cast<long long>(blockIdx.x) * I / C);
+            it_end = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * I / C);
+        }
     }
+    // one item's unit, first key and key count, and its tiles [t0, t1) of 64 selection entries
+    auto sparse_item = [&](int item, int& u, int& key0, int& nkeys, int& ta, int& tb) {
+        u = item / p.nchunks;
+        key0 = (item - u * p.nchunks) * kSparseChunkUnit;
+        nkeys = min(kSparseChunkUnit, p.width - key0);
+        ta = key0 / kTileKeys;
+        tb = (key0 + nkeys + kTileKeys - 1) / kTileKeys;
+    };
 
     if (warp >= kConsumerWarps) {
         // ================================================================ producer warps
         int it = 0;
         bool ok = true;
         if (VAR == kSparse) {
-            const int b = sp_u / p.Hkv;
             constexpr int NPW = Roles<VAR>::kProducerWarps;
             constexpr int kRowsPerWarp = kTileKeys / NPW;  // rows of a tile each producer warp copies
             const int ptid = threadIdx.x - kConsumerThreads;
@@ -921,44 +932,56 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             const bool isv = w >= CH;
             const int c = isv ? w - CH : w;
             const __nv_bfloat16* pool = isv ? p.v_pool : p.k_pool;
-            // this chunk's entries, read once (coalesced, all in flight) into shared memory with
-            // every entry outside [0, pool_rows) folded to -1
             int* sidx = sm.seq_prefix;
-            const int* selrow = p.sel + static_cast<size_t>(b) * p.width + sp_key0;
-            for (int i = ptid; i < sp_nkeys; i += 32 * NPW) {
-                const int idx = __ldg(selrow + i);
-                sidx[i] = (idx >= 0 && idx < p.pool_rows) ? idx : -1;
-            }
-            asm volatile("bar.sync 1, %0;" ::"r"(32 * NPW) : "memory");   // producer warps only
-            for (int t = t0; t < t1 && ok; ++t, ++it) {
-                const int s = it % S;
-                const uint32_t ph = (it / S) & 1;
-                if (!mbar_wait_warp(sm.empty + s, ph ^ 1u, sm.abort)) { ok = false; break; }
-                const int l0 = t * kTileKeys - sp_key0;
-                const int i0 = l0 + lane, i1 = l0 + 32 + lane;
-                const int idx0 = i0 < sp_nkeys ? sidx[i0] : -1;
-                const int idx1 = i1 < sp_nkeys ? sidx[i1] : -1;
-                const bool v0 = idx0 >= 0;
-                const bool v1 = idx1 >= 0;
-                const uint64_t mask = static_cast<uint64_t>(__ballot_sync(0xffffffffu, v0)) |
-                                      (static_cast<uint64_t>(__ballot_sync(0xffffffffu, v1)) << 32);
-                unsigned char* tile = sm.stages + s * Gm::kStageBytes + (isv ? Gm::kTileBytes : 0);
-                const int row_begin = pw * kRowsPerWarp;
-                const __nv_bfloat16* base = pool + static_cast<size_t>(sp_u) * p.pool_rows * D + c * 8;
-                // independent iterations: each lane reads its row's entry from shared memory, so
-                // the unrolled loop keeps several index reads and copies in flight
-#pragma unroll 8
-                for (int rb = row_begin; rb < row_begin + kRowsPerWarp; rb += kRowsPerInstr) {
-                    const int r = rb + sub;
-                    const int li = l0 + r;
-                    const int idx = li < sp_nkeys ? sidx[li] : -1;
-                    const bool valid = idx >= 0;
-                    const __nv_bfloat16* src = base + static_cast<size_t>(valid ? idx : 0) * D;
-                    cp_async_16(tile + tile_offset<Gm::kHalves>(r, c, 6), src, valid ? 16u : 0u);
+            for (int item = it_begin; item < it_end && ok; ++item) {
+                int sp_u, sp_key0, sp_nkeys, ta, tb;
+                sparse_item(item, sp_u, sp_key0, sp_nkeys, ta, tb);
+                const int b = sp_u / p.Hkv;
+                // every producer has issued the previous item's copies (their indices are in
+                // registers by then) before this item's entries replace them
+                asm volatile("bar.sync 1, %0;" ::"r"(32 * NPW) : "memory");
+                // this chunk's entries, read once (coalesced, all in flight) into shared memory
+                // with every entry outside [0, pool_rows) folded to -1
+                const int* selrow = p.sel + static_cast<size_t>(b) * p.width + sp_key0;
+                for (int i = ptid; i < sp_nkeys; i += 32 * NPW) {
+                    const int idx = __ldg(selrow + i);
+                    sidx[i] = (idx >= 0 && idx < p.pool_rows) ? idx : -1;
                 }
-                if (ptid == 0) sm.stage_mask[s] = mask;
-                cp_async_arrive_noinc(sm.full + s);
-                if (ptid == 0) mbar_arrive(sm.full + s);
+                asm volatile("bar.sync 1, %0;" ::"r"(32 * NPW) : "memory");   // producer warps only
+                const __nv_bfloat16* base =
+                    pool + static_cast<size_t>(sp_u) * p.pool_rows * D + c * 8;
+                for (int t = ta; t < tb; ++t, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = (it / S) & 1;
+                    if (!mbar_wait_warp(sm.empty + s, ph ^ 1u, sm.abort)) { ok = false; break; }
+                    const int l0 = t * kTileKeys - sp_key0;
+                    const int i0 = l0 + lane, i1 = l0 + 32 + lane;
+                    const int idx0 = i0 < sp_nkeys ? sidx[i0] : -1;
+                    const int idx1 = i1 < sp_nkeys ? sidx[i1] : -1;
+                    const bool v0 = idx0 >= 0;
+                    const bool v1 = idx1 >= 0;
+                    const uint64_t mask =
+                        static_cast<uint64_t>(__ballot_sync(0xffffffffu, v0)) |
+                        (static_cast<uint64_t>(__ballot_sync(0xffffffffu, v1)) << 32);
+                    unsigned char* tile =
+                        sm.stages + s * Gm::kStageBytes + (isv ? Gm::kTileBytes : 0);
+                    const int row_begin = pw * kRowsPerWarp;
+                    // independent iterations: each lane reads its row's entry from shared memory,
+                    // so the unrolled loop keeps several index reads and copies in flight
+#pragma unroll 8
+                    for (int rb = row_begin; rb < row_begin + kRowsPerWarp; rb += kRowsPerInstr) {
+                        const int r = rb + sub;
+                        const int li = l0 + r;
+                        const int idx = li < sp_nkeys ? sidx[li] : -1;
+                        const bool valid = idx >= 0;
+                        const __nv_bfloat16* src = base + static_cast<size_t>(valid ? idx : 0) * D;
+                        cp_async_16(tile + tile_offset<Gm::kHalves>(r, c, 6), src,
+                                    valid ? 16u : 0u);
+                    }
+                    if (ptid == 0) sm.stage_mask[s] = mask;
+                    cp_async_arrive_noinc(sm.full + s);
+                    if (ptid == 0) mbar_arrive(sm.full + s);
+                }
             }
             if (!ok) {
                 cp_async_wait_all();
@@ -1115,34 +1138,39 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 
     int it = 0;
     if (VAR == kSparse) {
-        Unit U;
-        U.u = sp_u;
-        U.b = sp_u / p.Hkv;
-        U.g = sp_u - U.b * p.Hkv;
-        U.len = p.width;
-        U.nt = 0;
-        U.base = 0;
-        U.hq0 = U.b * p.Hq + U.g * p.G;
-        U.nh = p.G;
-        U.cu = sp_u;
-        cs.load_q(p, U.hq0, U.nh);
-        cs.reset();
-        for (int t = t0; t < t1; ++t, ++it) {
-            const int s = it % S;
-            const uint32_t ph = (it / S) & 1;
-            if (!mbar_wait_warp(sm.full + s, ph, sm.abort)) {
-                *sm.abort = 1;
-                record_error(p.err, kErrWaitFull);
-                return;
+        for (int item = it_begin; item < it_end; ++item) {
+            int sp_u, sp_key0, sp_nkeys, ta, tb;
+            sparse_item(item, sp_u, sp_key0, sp_nkeys, ta, tb);
+            Unit U;
+            U.u = sp_u;
+            U.b = sp_u / p.Hkv;
+            U.g = sp_u - U.b * p.Hkv;
+            U.len = p.width;
+            U.nt = 0;
+            U.base = 0;
+            U.hq0 = U.b * p.Hq + U.g * p.G;
+            U.nh = p.G;
+            U.cu = sp_u;
+            cs.load_q(p, U.hq0, U.nh);
+            cs.reset();
+            for (int t = ta; t < tb; ++t, ++it) {
+                const int s = it % S;
+                const uint32_t ph = (it / S) & 1;
+                if (!mbar_wait_warp(sm.full + s, ph, sm.abort)) {
+                    *sm.abort = 1;
+                    record_error(p.err, kErrWaitFull);
+                    return;
+                }
+                const uint32_t ktile = smem_u32(sm.stages + s * Gm::kStageBytes);
+                cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2, 0, 0,
+                           0x7fffffff);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sm.empty + s);
             }
-            const uint32_t ktile = smem_u32(sm.stages + s * Gm::kStageBytes);
-            cs.consume(ktile, ktile + Gm::kTileBytes, sm.stage_mask[s], p.scale_log2, 0, 0,
-                       0x7fffffff);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sm.empty + s);
+            if (!finish_segment<D, GP>(p, sm, cs, U, p.nchunks == 1, item, sp_u * p.nchunks,
+                                       p.nchunks, gphase))
+                return;
         }
-        finish_segment<D, GP>(p, sm, cs, U, p.nchunks == 1, blockIdx.x, sp_u * p.nchunks,
-                              p.nchunks, gphase);
         return;
     }
 
