@@ -155,10 +155,11 @@ da_status decode_attn_paged_mq(const void *q, const void *k_pool, const void *v_
  * pads up to the fixed width); each valid entry adds its row once (duplicates count once per
  * entry); a -1 entry adds an exact zero to the denominator and nothing to the output.
  * Appending -1 pads to a selection leaves every output bit unchanged: the work is split into
- * chunks whose size depends on G = Hq / Hkv and D only, not on the width, B or the device.
- * 33 <= G <= 64 runs on the fifth-generation tensor cores (tcgen05, accumulators in tensor
- * memory), one CTA per (sequence and KV head, chunk of 512 entries) holding all G heads; G <= 32
- * runs on warp-level MMAs with chunks of 512 entries.
+ * chunks of 512 entries, a size that depends on nothing (not the width, B, G or the device), and
+ * each chunk is computed and merged the same way whichever CTA takes it.  33 <= G <= 64 runs on
+ * the fifth-generation tensor cores (tcgen05, accumulators in tensor memory), one CTA per
+ * (sequence and KV head, chunk) holding all G heads; G <= 32 runs on warp-level MMAs, one CTA
+ * per SM taking a contiguous range of whole chunks.
  *   1 <= pool_rows < 2^31; width >= 0 (width = 0 writes zeros).
  */
 da_status decode_attn_sparse(const void *q, const void *k_pool, const void *v_pool, void *out,

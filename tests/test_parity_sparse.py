@@ -175,6 +175,26 @@ def test_sparse_tensor_core_counters_return_to_zero(width):
     assert_close(out_f64(a), oracle_for(c), f"width {width}")
 
 
+@pytest.mark.parametrize("limit", [1, 2, 5, 7])
+def test_sparse_warp_mma_persistent_grid_is_assignment_free(limit):
+    """The warp-MMA sparse kernel runs a persistent grid: with 1..7 CTAs each takes a contiguous
+    range of whole (unit, chunk) items, finishing one while gathering the next, and merges units
+    split across CTAs.  Every item is computed the same way whichever CTA takes it, so the output
+    is bit-identical to the full grid's, and it matches the oracle."""
+    c = W.make_sparse(3, 32, 2, 128, 3000, 1700, 32, 400, seed=90 + limit, device=DEV,
+                      poison_unselected=True)
+    B_.decode_attn_set_grid_limit(0)
+    ref = B_.run_case(c)
+    B_.decode_attn_set_grid_limit(limit)
+    try:
+        out = B_.run_case(c)
+    finally:
+        B_.decode_attn_set_grid_limit(0)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert_close(out_f64(out), oracle_for(c), f"grid limit {limit}")
+
+
 def test_sparse_width_zero_gives_zeros():
     c = W.make_sparse(2, 8, 1, 128, 100, 8, 2, 0, seed=45, device=DEV)
     c.sel = c.sel[:, :0].contiguous()

@@ -255,6 +255,21 @@ def test_sparse_rows_read_with_multiplicity(Hq, Hkv, D, width, n_sel):
     check(out, reads, windows, B, Hq, Hkv, D, f"sparse G={Hq // Hkv} D={D} width={width}")
 
 
+@pytest.mark.parametrize("limit", [1, 3])
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 2, 128), (8, 2, 64)], ids=lambda x: str(x))
+def test_sparse_rows_read_on_few_ctas(Hq, Hkv, D, limit):
+    """The warp-MMA sparse kernel with 1 or 3 CTAs, each taking many (unit, chunk) items in a row:
+    every item still reads exactly its own rows."""
+    B_.decode_attn_set_grid_limit(limit)
+    rng = np.random.default_rng(limit * 31 + D)
+    pool_rows = 1024
+    sel_row = selection(1100, pool_rows, 1025, rng)
+    B = -(-pool_rows // D) // Hkv
+    c, reads, windows = sparse_case(B, Hq, Hkv, D, pool_rows, sel_row)
+    out = B_.run_case(c)
+    check(out, reads, windows, B, Hq, Hkv, D, f"sparse G={Hq // Hkv} D={D} grid={limit}")
+
+
 @pytest.mark.parametrize("name", ["sparse_selected", "sparse_selected_g16"])
 def test_sparse_named_workload_rows_read(name):
     """At the named workloads' full shape (width 2048, 65536 pool rows, the launch the benchmark
