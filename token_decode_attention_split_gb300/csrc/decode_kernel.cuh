@@ -727,12 +727,14 @@ __device__ __forceinline__ bool merge_unit(const Params& p, const SmemPtrs& sm, 
 }
 
 // Finishes one segment of unit U: merges the key-split warps, then either stores the output or
-// publishes a partial and, in the CTA that completes the unit, merges all partials.
+// publishes a partial and, in the CTA that completes the unit, merges all partials.  With
+// `defer`, a partial is only stored: the caller counts it on the unit's counter later
+// (publish_and_merge).
 template <int D, int GP, class CS>
 __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& sm,
                                                CS& cs, const Unit& U,
                                                bool whole, int seg, int first_seg, int nseg,
-                                               uint32_t& gphase) {
+                                               uint32_t& gphase, bool defer = false) {
     using Gm = Geometry<D, GP>;
     const int tid = threadIdx.x;   // 0..127 (consumers)
     cs.stash(sm);
@@ -799,7 +801,7 @@ __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& 
         }
     }
     if (!whole && tid < U.nh) p.part_lse[static_cast<size_t>(seg) * SH + tid] = sm.head_lse[tid];
-    if (!whole) {
+    if (!whole && !defer) {
         // The group barrier orders every consumer's partial-row stores before thread 0's
         // release on the unit's counter; the CTA that takes the counter to nseg acquires all
         // segments' rows there, and the next group barrier hands that on to its other threads.
@@ -815,6 +817,52 @@ __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& 
         }
     }
     return group_sync(sm, gphase, p.err);
+}
+
+// Counts the segments a CTA stored with finish_segment(..., defer) on their units' counters --
+// the items [it_begin, it_end) of nchunks segments per unit, all published by one acquire-release
+// add per unit, the units taken by the CTA's threads side by side -- and merges every unit this
+// CTA completes, in unit order, with merge_unit (segment order within a unit, so the result does
+// not depend on which CTA completes it).  The caller's last group barrier orders every partial
+// store before these releases.  `flags` is scratch for kConsumerThreads ints.
+template <int D, int GP>
+__device__ __forceinline__ bool publish_and_merge(const Params& p, const SmemPtrs& sm, int* flags,
+                                                  int it_begin, int it_end, uint32_t& gphase) {
+    const int tid = threadIdx.x;
+    const int nck = p.nchunks;
+    const int u_first = it_begin / nck, u_last = (it_end - 1) / nck;
+    for (int u0 = u_first; u0 <= u_last; u0 += kConsumerThreads) {
+        const int u = u0 + tid;
+        int last = 0;
+        if (u <= u_last) {
+            const int lo = max(it_begin, u * nck), hi = min(it_end, (u + 1) * nck);
+            const unsigned n = static_cast<unsigned>(hi - lo);
+            unsigned prev;
+            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                         : "=r"(prev) : "l"(p.counters + u), "r"(n) : "memory");
+            last = prev + n == static_cast<unsigned>(nck) ? 1 : 0;
+        }
+        flags[tid] = last;
+        if (!group_sync(sm, gphase, p.err)) return false;
+        const int nu = min(kConsumerThreads, u_last - u0 + 1);
+        for (int i = 0; i < nu; ++i) {
+            if (!flags[i]) continue;
+            Unit U;
+            U.u = u0 + i;
+            U.b = U.u / p.Hkv;
+            U.g = U.u - U.b * p.Hkv;
+            U.len = p.width;
+            U.nt = 0;
+            U.base = 0;
+            U.hq0 = U.b * p.Hq + U.g * p.G;
+            U.nh = p.G;
+            U.cu = U.u;
+            if (!merge_unit<D, GP>(p, sm, U, U.u * nck, nck, gphase)) return false;
+            if (tid == 0) p.counters[U.cu] = 0u;
+        }
+        if (!group_sync(sm, gphase, p.err)) return false;   // flags reused
+    }
+    return true;
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -932,22 +980,44 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             const bool isv = w >= CH;
             const int c = isv ? w - CH : w;
             const __nv_bfloat16* pool = isv ? p.v_pool : p.k_pool;
-            int* sidx = sm.seq_prefix;
-            for (int item = it_begin; item < it_end && ok; ++item) {
+            // an item's entries, read once (coalesced, all in flight) with every entry outside
+            // [0, pool_rows) folded to -1, go to one of two index buffers: the next item's are
+            // fetched into registers while this item's copies are issued, so no item waits for
+            // its indices
+            constexpr int kIdxPer = kSparseChunkUnit / (32 * NPW);   // entries per producer thread
+            static_assert(kIdxPer * 32 * NPW == kSparseChunkUnit, "chunk split over producers");
+            static_assert(2 * kSparseChunkUnit <= kMaxPagedBatch + 2, "two index buffers fit");
+            int nidx[kIdxPer];
+            auto fetch_idx = [&](int item) {
+                int u, key0, nkeys, ta, tb;
+                sparse_item(item, u, key0, nkeys, ta, tb);
+                const int* selrow = p.sel + static_cast<size_t>(u / p.Hkv) * p.width + key0;
+#pragma unroll
+                for (int k = 0; k < kIdxPer; ++k) {
+                    const int i = ptid + k * 32 * NPW;
+                    const int idx = i < nkeys ? __ldg(selrow + i) : -1;
+                    nidx[k] = (idx >= 0 && idx < p.pool_rows) ? idx : -1;
+                }
+            };
+            auto store_idx = [&](int* buf) {
+#pragma unroll
+                for (int k = 0; k < kIdxPer; ++k) buf[ptid + k * 32 * NPW] = nidx[k];
+            };
+            if (it_begin < it_end) {
+                fetch_idx(it_begin);
+                store_idx(sm.seq_prefix);
+            }
+            // every producer warp passes every item's barrier, also after one of its waits gave
+            // up (it then issues nothing), so no warp is left waiting at a barrier
+            for (int item = it_begin; item < it_end; ++item) {
                 int sp_u, sp_key0, sp_nkeys, ta, tb;
                 sparse_item(item, sp_u, sp_key0, sp_nkeys, ta, tb);
-                const int b = sp_u / p.Hkv;
-                // every producer has issued the previous item's copies (their indices are in
-                // registers by then) before this item's entries replace them
-                asm volatile("bar.sync 1, %0;" ::"r"(32 * NPW) : "memory");
-                // this chunk's entries, read once (coalesced, all in flight) into shared memory
-                // with every entry outside [0, pool_rows) folded to -1
-                const int* selrow = p.sel + static_cast<size_t>(b) * p.width + sp_key0;
-                for (int i = ptid; i < sp_nkeys; i += 32 * NPW) {
-                    const int idx = __ldg(selrow + i);
-                    sidx[i] = (idx >= 0 && idx < p.pool_rows) ? idx : -1;
-                }
+                int* sidx = sm.seq_prefix + ((item - it_begin) & 1) * kSparseChunkUnit;
+                // this item's entries are stored, and every producer has issued the previous
+                // item's copies (which read the other buffer)
                 asm volatile("bar.sync 1, %0;" ::"r"(32 * NPW) : "memory");   // producer warps only
+                if (!ok) continue;
+                if (item + 1 < it_end) fetch_idx(item + 1);
                 const __nv_bfloat16* base =
                     pool + static_cast<size_t>(sp_u) * p.pool_rows * D + c * 8;
                 for (int t = ta; t < tb; ++t, ++it) {
@@ -982,6 +1052,8 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                     cp_async_arrive_noinc(sm.full + s);
                     if (ptid == 0) mbar_arrive(sm.full + s);
                 }
+                if (item + 1 < it_end)
+                    store_idx(sm.seq_prefix + ((item + 1 - it_begin) & 1) * kSparseChunkUnit);
             }
             if (!ok) {
                 cp_async_wait_all();
@@ -1167,10 +1239,13 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sm.empty + s);
             }
+            // a partial is only stored here; its unit's counter is bumped after the last item
             if (!finish_segment<D, GP>(p, sm, cs, U, p.nchunks == 1, item, sp_u * p.nchunks,
-                                       p.nchunks, gphase))
+                                       p.nchunks, gphase, true))
                 return;
         }
+        if (p.nchunks > 1 && it_begin < it_end)
+            publish_and_merge<D, GP>(p, sm, sm.seq_len, it_begin, it_end, gphase);
         return;
     }
 
