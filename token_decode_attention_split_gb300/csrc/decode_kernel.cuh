@@ -943,16 +943,21 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         t0 = static_cast<int>(static_cast<long long>(blockIdx.x) * N / C);
         t1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * N / C);
     }
-    // sparse: the items (unit u, chunk) are numbered u * nchunks + chunk; CTA c takes the
-    // contiguous range [c * I / C, (c + 1) * I / C) of the I items, each a whole chunk (so a
-    // chunk boundary never moves) finished as its own segment
+    // sparse: the items (unit u, chunk) are numbered u * nchunks + chunk; CTA c takes a
+    // contiguous range of them, each a whole chunk (so a chunk boundary never moves) finished as
+    // its own segment.  With I = q * C + r, the first r CTAs take q + 1 items and the rest q, the
+    // longer ranges first: when q + 1 is the chunk count, each longer range is one whole unit,
+    // which that CTA merges by itself, and the merges of units split across CTAs fall to the
+    // CTAs that finish a whole item earlier.
     int it_begin = 0, it_end = 0;
     if (VAR == kSparse) {
         const int I = p.B * p.Hkv * p.nchunks;
         C = min(static_cast<int>(gridDim.x), I);
-        if (static_cast<int>(blockIdx.x) < C) {
-            it_begin = static_cast<int>(static_cast<long long>(blockIdx.x) * I / C);
-            it_end = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * I / C);
+        const int c = static_cast<int>(blockIdx.x);
+        if (c < C) {
+            const int q = I / C, r = I - q * C;
+            it_begin = c < r ? c * (q + 1) : r * (q + 1) + (c - r) * q;
+            it_end = it_begin + (c < r ? q + 1 : q);
         }
     }
     // one item's unit, first key and key count, and its tiles [t0, t1) of 64 selection entries
