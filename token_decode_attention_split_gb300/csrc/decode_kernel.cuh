@@ -823,8 +823,10 @@ __device__ __forceinline__ bool finish_segment(const Params& p, const SmemPtrs& 
 // the items [it_begin, it_end) of nchunks segments per unit, all published by one acquire-release
 // add per unit, the units taken by the CTA's threads side by side -- and merges every unit this
 // CTA completes, in unit order, with merge_unit (segment order within a unit, so the result does
-// not depend on which CTA completes it).  The caller's last group barrier orders every partial
-// store before these releases.  `flags` is scratch for kConsumerThreads ints.
+// not depend on which CTA completes it).  A unit whose every segment this CTA stored is merged
+// without touching its counter; a GPU-scope fence then makes those partial rows visible to the
+// merge's L2 loads.  The caller's last group barrier orders every partial store before these
+// releases and fences.  `flags` is scratch for kConsumerThreads ints.
 template <int D, int GP>
 __device__ __forceinline__ bool publish_and_merge(const Params& p, const SmemPtrs& sm, int* flags,
                                                   int it_begin, int it_end, uint32_t& gphase) {
@@ -837,10 +839,15 @@ __device__ __forceinline__ bool publish_and_merge(const Params& p, const SmemPtr
         if (u <= u_last) {
             const int lo = max(it_begin, u * nck), hi = min(it_end, (u + 1) * nck);
             const unsigned n = static_cast<unsigned>(hi - lo);
-            unsigned prev;
-            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
-                         : "=r"(prev) : "l"(p.counters + u), "r"(n) : "memory");
-            last = prev + n == static_cast<unsigned>(nck) ? 1 : 0;
+            if (n == static_cast<unsigned>(nck)) {
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                last = 1;
+            } else {
+                unsigned prev;
+                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                             : "=r"(prev) : "l"(p.counters + u), "r"(n) : "memory");
+                last = prev + n == static_cast<unsigned>(nck) ? 1 : 0;
+            }
         }
         flags[tid] = last;
         if (!group_sync(sm, gphase, p.err)) return false;
@@ -858,6 +865,7 @@ __device__ __forceinline__ bool publish_and_merge(const Params& p, const SmemPtr
             U.nh = p.G;
             U.cu = U.u;
             if (!merge_unit<D, GP>(p, sm, U, U.u * nck, nck, gphase)) return false;
+            // (a unit merged without its counter left it at zero)
             if (tid == 0) p.counters[U.cu] = 0u;
         }
         if (!group_sync(sm, gphase, p.err)) return false;   // flags reused
