@@ -175,6 +175,27 @@ def test_sparse_tensor_core_counters_return_to_zero(width):
     assert_close(out_f64(a), oracle_for(c), f"width {width}")
 
 
+@pytest.mark.parametrize("limit", [0, 1, 5, 7])
+def test_sparse_warp_mma_counters_return_to_zero(limit):
+    """The warp-MMA kernel's merge counters (one word per unit) are zero after every call,
+    whether a CTA computed all of a unit (merged without its counter: every unit with one CTA,
+    some with five or seven) or the unit was split across CTAs (counted, then reset by the
+    merging CTA: every unit with the full grid of one item per CTA, the others with five or
+    seven); a second call on the same workspace gives the same bits, which match the oracle."""
+    c = W.make_sparse(3, 32, 2, 128, 3000, 2000, 32, 300, seed=170 + limit, device=DEV)
+    ws = B_.new_workspace(B_.decode_attn_workspace_size(2, c.B, c.Hq, c.Hkv, c.D, c.width), DEV)
+    B_.decode_attn_set_grid_limit(limit)
+    try:
+        a = B_.run_case(c, workspace=ws)
+        b = B_.run_case(c, workspace=ws)
+    finally:
+        B_.decode_attn_set_grid_limit(0)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert torch.count_nonzero(ws[: 4 * c.B * c.Hkv]).item() == 0
+    assert_close(out_f64(a), oracle_for(c), f"grid limit {limit}")
+
+
 @pytest.mark.parametrize("limit", [1, 2, 5, 7])
 def test_sparse_warp_mma_persistent_grid_is_assignment_free(limit):
     """The warp-MMA sparse kernel runs a persistent grid: with 1..7 CTAs each takes a contiguous
