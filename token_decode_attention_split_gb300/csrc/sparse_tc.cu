@@ -12,12 +12,16 @@
 // merged across CTAs by log-sum-exp exactly as in the mma.sync kernel (partial rows, a per-unit
 // counter, the last CTA merges in segment order).
 //
-// Inside a CTA (288 threads):
-//   warps 5-8  producers: gather the chunk's selected K and V rows with 16-byte cp.async into a
-//              128 KB ring of stages (64 rows of K and of V each: 4 stages at D = 128, 8 at
-//              D = 64; 128-byte swizzle; rows outside [0, pool_rows) zero-filled); a stage's
-//              full barrier completes when every producer thread's copies for it have landed
-//              (cp.async.mbarrier.arrive), so the producers run ahead as far as the ring allows;
+// Inside a CTA (12 warps; warp w issues on the SM's scheduler w % 4, and the two softmax warps
+// that hold heads run on schedulers 0 and 1, so the producers are warps 6, 7, 10 and 11, on
+// schedulers 2 and 3 — 2.3% faster per call than sharing the softmax warps' schedulers — and
+// warps 5, 8 and 9 exit after the set-up):
+//   warps 6, 7, 10, 11  producers: gather the chunk's selected K and V rows with 16-byte
+//              cp.async into a 128 KB ring of stages (64 rows of K and of V each: 4 stages at
+//              D = 128, 8 at D = 64; 128-byte swizzle; rows outside [0, pool_rows)
+//              zero-filled); a stage's full barrier completes when every producer thread's
+//              copies for it have landed (cp.async.mbarrier.arrive), so the producers run ahead
+//              as far as the ring allows;
 //   warp 4     allocates 256 TMEM columns; one lane issues S(t) = Q K(t)^T into one of two
 //              64-column S buffers and O += P(t) V(t) into the D-column O accumulator (after
 //              acquiring a stage it fences the generic proxy, in which cp.async wrote the rows,
@@ -47,7 +51,8 @@ constexpr int kTcPBytes = kTcM * kTileKeys * 2;  // [128 rows][128 B]: one tile'
 constexpr int kTcSoftmaxWarps = 4;
 constexpr int kTcMmaWarp = 4;
 constexpr int kTcProducerWarps = 4;
-constexpr int kTcThreads = 32 * (kTcSoftmaxWarps + 1 + kTcProducerWarps);
+constexpr int kTcThreads = 32 * 12;               // producers on warps 6, 7, 10, 11 (see above)
+static_assert(kTcProducerWarps == 4, "the producers are warps 6, 7, 10 and 11");
 constexpr uint32_t kTcCols = 256;                // TMEM: S buffers at columns 0 and 64, O at 128
 constexpr uint32_t kTcColO = 128;
 constexpr float kTcRescaleLog2 = 8.f;
@@ -302,8 +307,9 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CU
 
     if (warp > kTcMmaWarp) {
         // ============================================================ producer warps
-        const int ptid = threadIdx.x - 32 * (kTcMmaWarp + 1);
-        const int pw = ptid >> 5;
+        if ((warp & 3) < 2) return;                          // warps 5, 8, 9: no role
+        const int pw = (warp & 1) + ((warp >> 3) << 1);      // warps 6, 7, 10, 11 -> 0..3
+        const int ptid = pw * 32 + lane;
         const int* selrow = p.sel + static_cast<size_t>(b) * p.width + key0;
         for (int i = ptid; i < nkeys; i += 32 * kTcProducerWarps) {
             const int idx = __ldg(selrow + i);
