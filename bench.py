@@ -514,8 +514,8 @@ def run_reference(args, world, rank):
         gbs = c.algorithmic_bytes() / secs_full / 1e9
         ms = secs_full * 1e3
         cores, dtype = threads, "f64"
-        sample = (f"{rows_used} of {c.B * c.Hq} (b, h) rows per step, scaled to the whole "
-                  f"workload")
+        sample = (f"{rows_used} (b, h) row computations per step (a call has {c.B * c.Hq} rows; "
+                  f"a shorter sample is repeated in whole passes), scaled to the whole workload")
         cfg = workload_config(name, algorithmic_bytes_per_call=int(c.algorithmic_bytes()),
                               l2=l2_note(c), parallelism=f"replicas x{world}")
     line = {
