@@ -882,7 +882,13 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     extern __shared__ unsigned char smem_raw[];
     const SmemPtrs sm = carve_smem<D, GP>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int S = Gm::kStages;
+    // Stages of the ring in use.  Dense units of up to 8 query columns stream fastest with 128 KB
+    // in flight per SM (four 32 KB stages at D = 128: dense_long 317.5 -> 296.1 us against the
+    // six that fit, dense_batched 42.6 -> 41.3 us; three are slower again); heavier consumers
+    // (more columns) and the paged and sparse gathers keep every stage that fits.
+    constexpr int kDenseRing = 128 * 1024 / Gm::kStageBytes;
+    constexpr int S = (VAR == kDense && GP <= 8 && kDenseRing < Gm::kStages) ? kDenseRing
+                                                                            : Gm::kStages;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
