@@ -882,13 +882,16 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     extern __shared__ unsigned char smem_raw[];
     const SmemPtrs sm = carve_smem<D, GP>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Stages of the ring in use.  Dense units of up to 8 query columns stream fastest with 128 KB
-    // in flight per SM (four 32 KB stages at D = 128: dense_long 317.5 -> 296.1 us against the
-    // six that fit, dense_batched 42.6 -> 41.3 us; three are slower again); heavier consumers
-    // (more columns) and the paged and sparse gathers keep every stage that fits.
-    constexpr int kDenseRing = 128 * 1024 / Gm::kStageBytes;
-    constexpr int S = (VAR == kDense && GP <= 8 && kDenseRing < Gm::kStages) ? kDenseRing
-                                                                            : Gm::kStages;
+    // Stages of the ring in use: more rows in flight than a stream needs only lengthen the memory
+    // queues.  Dense units of up to 8 query columns stream fastest with 128 KB in flight per SM
+    // (four 32 KB stages at D = 128: dense_long 317.5 -> 296.1 us against the six that fit,
+    // dense_batched 42.6 -> 41.3 us; three are slower again), the paged gather with 160 KB
+    // (paged_ragged_p64 603.0 -> 588.6 us with five stages instead of six; four: 595.7);
+    // heavier dense consumers (more columns) and the sparse gathers keep every stage that fits.
+    constexpr int kRingCap = (VAR == kDense && GP <= 8) ? 128 * 1024 / Gm::kStageBytes
+                             : VAR == kPaged            ? 160 * 1024 / Gm::kStageBytes
+                                                        : Gm::kStages;
+    constexpr int S = kRingCap < Gm::kStages ? kRingCap : Gm::kStages;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
